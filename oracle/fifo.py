@@ -1,0 +1,641 @@
+"""FIFO protocol state machines (CPU oracle; test infrastructure only).
+
+Each endpoint is an explicit state machine over shared FIFO state.  A seeded
+scheduler (`run`) fires one enabled event at a time; `explore` walks every
+reachable state of a tiny system.  After every event the FIFO invariants are
+checked, so a schedule that breaks the protocol raises `ProtocolViolation`
+at the event that broke it.
+
+Protocol sources (page title, section):
+* copy mode: "NCCL transport data transfer (二)", p2pTransport / copy mode —
+  the sender writes a slot, updates tail; the receiver sees tail, copies the
+  slot to the user buffer, updates head.  "NCCL transport setup",
+  整体图解 (producer/consumer model) says the same.
+* zero copy: same page, zero copy — the receiver puts its buffer address in
+  ptrExchange, the sender reads it, writes the data there, updates tail; the
+  receiver sees tail and updates head.
+* shm normal mode (host-placed FIFO): same page, shmTransport / 正常方式 —
+  identical steps with the buffers and tail in host memory.
+* LL: "RDMA and GPUDirect" §4.1 — the data carries the flag and the receiver
+  polls memory.  Line = 16 bytes {data0, flag0, data1, flag1}.
+* initial counters: "NCCL transport setup", netTransport (head starts at 0
+  outside shared-buffer mode) and the per-slot size word initialised to -1.
+
+Readings where the pages are silent:
+* credit: the sender may fill step s only while s < head + N;
+* LL flag of every line of slot-step s is (s + 1) mod 2**32, so that zeroed
+  memory never matches; LL still uses head for slot reuse and has no tail;
+* each 8-byte half {data, flag} of an LL line becomes visible on its own
+  (a 16-byte line may be seen torn), in any order within a small window;
+* zero copy: the receiver posts its address only into an empty ptrExchange;
+  the sender writes chunks of at most S bytes, one tail per chunk, under the
+  same credit rule; the receiver returns head per chunk; the sender empties
+  ptrExchange once head reaches the last chunk.
+"""
+from __future__ import annotations
+
+import copy
+from dataclasses import dataclass
+
+import numpy as np
+
+from .partition import ceil_div
+
+
+class ProtocolViolation(AssertionError):
+    """A schedule broke a FIFO invariant."""
+
+
+class Deadlock(AssertionError):
+    """No endpoint can move but some have not finished."""
+
+
+# --------------------------------------------------------------------------
+# SIMPLE
+# --------------------------------------------------------------------------
+
+class SimpleFifo:
+    """Shared state of one SIMPLE channel: N slots of S bytes, head, tail."""
+
+    def __init__(self, nslots: int, slot_bytes: int, step0: int = 0):
+        if nslots < 1 or slot_bytes < 1:
+            raise ValueError("need nslots >= 1 and slot_bytes >= 1")
+        self.N = nslots
+        self.S = slot_bytes
+        self.slots = np.zeros((nslots, slot_bytes), np.uint8)
+        self.size = [-1] * nslots          # per-slot size word
+        self.head = step0                  # consumer cursor (credit)
+        self.tail = step0                  # producer cursor
+        # bookkeeping used only by the checks:
+        self.owner = [None] * nslots       # step whose bytes the slot holds
+        self.consumed = [True] * nslots
+        self.max_occupancy = 0
+
+    def check(self):
+        occ = self.tail - self.head
+        if occ < 0:
+            raise ProtocolViolation(f"head {self.head} passed tail {self.tail}")
+        if occ > self.N:
+            raise ProtocolViolation(f"tail {self.tail} exceeds head {self.head} + N {self.N}")
+        self.max_occupancy = max(self.max_occupancy, occ)
+
+    def state(self):
+        return (self.head, self.tail, self.slots.tobytes(), tuple(self.size),
+                tuple(self.owner), tuple(self.consumed))
+
+    # slot access with ownership checks
+    def fill(self, step: int, data: np.ndarray):
+        k = step % self.N
+        if not self.consumed[k]:
+            raise ProtocolViolation(f"step {step} overwrites slot {k} holding unconsumed step {self.owner[k]}")
+        self.slots[k, :len(data)] = data
+        self.size[k] = len(data)
+        self.owner[k] = step
+        self.consumed[k] = False
+
+    def drain(self, step: int, nbytes: int) -> np.ndarray:
+        k = step % self.N
+        if self.owner[k] != step or self.consumed[k]:
+            raise ProtocolViolation(f"step {step} reads slot {k} holding step {self.owner[k]} "
+                                    f"(consumed={self.consumed[k]})")
+        if self.size[k] != nbytes:
+            raise ProtocolViolation(f"slot {k} size word {self.size[k]} != {nbytes}")
+        self.consumed[k] = True
+        return self.slots[k, :nbytes].copy()
+
+
+class Actor:
+    name = "actor"
+
+    def done(self) -> bool:
+        raise NotImplementedError
+
+    def choices(self) -> list:
+        raise NotImplementedError
+
+    def fire(self, choice):
+        raise NotImplementedError
+
+    def state(self):
+        raise NotImplementedError
+
+
+class SimpleSender(Actor):
+    """Copy src[lo:hi] into the FIFO one slot-step at a time.
+
+    Events per step: wait credit (step < head + N) -> fill slot -> store tail.
+    `fault` plants a mistake for the checker tests: "skip_credit",
+    "tail_before_fill", "skip_tail" (last step's tail never stored).
+    """
+    WAIT, FILL, PUB, DONE = range(4)
+
+    def __init__(self, fifo: SimpleFifo, src: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.f, self.src, self.lo, self.hi = fifo, src, lo, hi
+        self.base = fifo.tail
+        self.nsteps = ceil_div(hi - lo, fifo.S)
+        self.step = self.base
+        self.phase = self.WAIT if self.nsteps else self.DONE
+        self.fault = fault
+        self.name = f"simple-send[{lo}:{hi}]"
+        if fault == "tail_before_fill":
+            self.order = (self.WAIT, self.PUB, self.FILL)
+        else:
+            self.order = (self.WAIT, self.FILL, self.PUB)
+
+    def _piece(self):
+        off = self.lo + (self.step - self.base) * self.f.S
+        return self.src[off:min(self.hi, off + self.f.S)]
+
+    def done(self):
+        return self.phase == self.DONE
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT:
+            ok = self.fault == "skip_credit" or self.step < self.f.head + self.f.N
+            return [0] if ok else []
+        if self.phase == self.PUB and self.fault == "skip_tail" and self.step == self.base + self.nsteps - 1:
+            return []
+        return [0]
+
+    def _advance(self):
+        i = self.order.index(self.phase)
+        if i + 1 < len(self.order):
+            self.phase = self.order[i + 1]
+        else:
+            self.step += 1
+            self.phase = self.WAIT if self.step < self.base + self.nsteps else self.DONE
+
+    def fire(self, choice):
+        if self.phase == self.FILL:
+            self.f.fill(self.step, self._piece())
+        elif self.phase == self.PUB:
+            self.f.tail = self.step + 1
+        self._advance()
+
+    def state(self):
+        return (self.step, self.phase)
+
+
+class SimpleReceiver(Actor):
+    """Copy the FIFO's slot-steps into dst[lo:hi].
+
+    Events per step: wait tail > step -> copy slot out -> store head.
+    `fault`: "head_before_copy", "skip_tail_wait".
+    """
+    WAIT, COPY, PUB, DONE = range(4)
+
+    def __init__(self, fifo: SimpleFifo, dst: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.f, self.dst, self.lo, self.hi = fifo, dst, lo, hi
+        self.base = fifo.head
+        self.nsteps = ceil_div(hi - lo, fifo.S)
+        self.step = self.base
+        self.phase = self.WAIT if self.nsteps else self.DONE
+        self.fault = fault
+        self.name = f"simple-recv[{lo}:{hi}]"
+        if fault == "head_before_copy":
+            self.order = (self.WAIT, self.PUB, self.COPY)
+        else:
+            self.order = (self.WAIT, self.COPY, self.PUB)
+
+    def done(self):
+        return self.phase == self.DONE
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT:
+            ok = self.fault == "skip_tail_wait" or self.f.tail > self.step
+            return [0] if ok else []
+        return [0]
+
+    def _advance(self):
+        i = self.order.index(self.phase)
+        if i + 1 < len(self.order):
+            self.phase = self.order[i + 1]
+        else:
+            self.step += 1
+            self.phase = self.WAIT if self.step < self.base + self.nsteps else self.DONE
+
+    def fire(self, choice):
+        if self.phase == self.COPY:
+            off = self.lo + (self.step - self.base) * self.f.S
+            n = min(self.hi, off + self.f.S) - off
+            self.dst[off:off + n] = self.f.drain(self.step, n)
+        elif self.phase == self.PUB:
+            self.f.head = self.step + 1
+        self._advance()
+
+    def state(self):
+        return (self.step, self.phase)
+
+
+# --------------------------------------------------------------------------
+# LL
+# --------------------------------------------------------------------------
+
+LL_LINE_BYTES = 16      # {data0, flag0, data1, flag1}, uint32 each
+LL_LINE_PAYLOAD = 8     # two uint32 data words per line
+
+
+def ll_flag(step: int) -> int:
+    return (step + 1) & 0xFFFFFFFF
+
+
+class LLFifo:
+    """Shared state of one LL channel: N slots of S bytes of 16-byte lines."""
+
+    def __init__(self, nslots: int, slot_bytes: int, step0: int = 0):
+        if nslots < 1 or slot_bytes < LL_LINE_BYTES or slot_bytes % LL_LINE_BYTES:
+            raise ValueError("LL slots hold whole 16-byte lines")
+        self.N = nslots
+        self.S = slot_bytes
+        self.L = slot_bytes // LL_LINE_BYTES
+        self.lines = np.zeros((nslots, self.L, 4), np.uint32)      # visible memory
+        self.half_owner = np.full((nslots, self.L, 2), -1, np.int64)  # bookkeeping
+        self.head = step0
+        self.started = step0          # steps the sender has been granted (bookkeeping)
+        self.max_occupancy = 0
+
+    def check(self):
+        occ = self.started - self.head
+        if occ < 0 or occ > self.N:
+            raise ProtocolViolation(f"LL sender started {self.started} steps, head {self.head}, N {self.N}")
+        self.max_occupancy = max(self.max_occupancy, occ)
+
+    def state(self):
+        return (self.head, self.started, self.lines.tobytes(), self.half_owner.tobytes())
+
+
+@dataclass
+class _Half:
+    slot: int
+    line: int
+    half: int
+    data: int
+    flag: int
+    step: int
+
+
+class LLSender(Actor):
+    """Send words[lo:hi] (uint32, even count) as LL lines.
+
+    Events: wait credit for a new slot-step; issue the next line (its two
+    8-byte halves enter a pending pool of at most `window` lines); make any
+    pending half visible.  `fault`: "skip_credit".
+    """
+
+    def __init__(self, fifo: LLFifo, words: np.ndarray, lo: int, hi: int, window: int = 2,
+                 fault: str | None = None):
+        if (hi - lo) % 2:
+            raise ValueError("LL moves whole 8-byte lines")
+        self.f, self.words, self.lo, self.hi = fifo, words, lo, hi
+        self.nlines = (hi - lo) // 2
+        self.base = fifo.started
+        self.nsteps = ceil_div(self.nlines, fifo.L)
+        self.step = self.base          # next step to start
+        self.line = 0                  # next line within the current step
+        self.granted = False
+        self.pending: list[_Half] = []
+        self.window = window
+        self.fault = fault
+        self.name = f"ll-send[{lo}:{hi}]"
+
+    def _lines_in(self, step):
+        rel = step - self.base
+        return min(self.f.L, self.nlines - rel * self.f.L)
+
+    def done(self):
+        return self.step >= self.base + self.nsteps and not self.pending
+
+    def choices(self):
+        opts = [("vis", i) for i in range(len(self.pending))]
+        if self.step < self.base + self.nsteps:
+            if not self.granted:
+                if self.fault == "skip_credit" or self.step < self.f.head + self.f.N:
+                    opts.append(("grant",))
+            elif len(self.pending) < 2 * self.window:
+                opts.append(("issue",))
+        return opts
+
+    def fire(self, choice):
+        if choice[0] == "grant":
+            self.granted = True
+            self.f.started = self.step + 1
+        elif choice[0] == "issue":
+            rel = self.step - self.base
+            g = rel * self.f.L + self.line            # global line index
+            d0 = int(self.words[self.lo + 2 * g])
+            d1 = int(self.words[self.lo + 2 * g + 1])
+            k = self.step % self.f.N
+            fl = ll_flag(self.step)
+            self.pending.append(_Half(k, self.line, 0, d0, fl, self.step))
+            self.pending.append(_Half(k, self.line, 1, d1, fl, self.step))
+            self.line += 1
+            if self.line == self._lines_in(self.step):
+                self.step += 1
+                self.line = 0
+                self.granted = False
+        else:
+            h = self.pending.pop(choice[1])
+            if h.step >= self.f.head + self.f.N:
+                raise ProtocolViolation(f"LL step {h.step} overwrites slot {h.slot} before head {self.f.head}")
+            self.f.lines[h.slot, h.line, 2 * h.half] = h.data
+            self.f.lines[h.slot, h.line, 2 * h.half + 1] = h.flag
+            self.f.half_owner[h.slot, h.line, h.half] = h.step
+
+    def state(self):
+        return (self.step, self.line, self.granted,
+                tuple((h.slot, h.line, h.half, h.data, h.flag, h.step) for h in self.pending))
+
+
+class LLReceiver(Actor):
+    """Receive LL lines into out[lo:hi]; head = step + 1 after a slot's last line.
+
+    A line is accepted only when both flags equal the step's flag.
+    `fault`: "one_flag" (accept on flag1 alone), "head_early" (return credit
+    before reading the slot's last line).
+    """
+
+    def __init__(self, fifo: LLFifo, out: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.f, self.out, self.lo, self.hi = fifo, out, lo, hi
+        self.nlines = (hi - lo) // 2
+        self.base = fifo.head
+        self.nsteps = ceil_div(self.nlines, fifo.L)
+        self.step = self.base
+        self.line = 0
+        self.pub = False               # all lines of `step` read, head not yet stored
+        self.early = False             # planted fault: head already stored for `step`
+        self.fault = fault
+        self.name = f"ll-recv[{lo}:{hi}]"
+
+    def _lines_in(self, step):
+        rel = step - self.base
+        return min(self.f.L, self.nlines - rel * self.f.L)
+
+    def done(self):
+        return self.step >= self.base + self.nsteps
+
+    def choices(self):
+        if self.done():
+            return []
+        if self.pub:
+            return [("head",)]
+        if (self.fault == "head_early" and not self.early
+                and self.line == self._lines_in(self.step) - 1):
+            return [("head",)]
+        k = self.step % self.f.N
+        ln = self.f.lines[k, self.line]
+        fl = ll_flag(self.step)
+        if self.fault == "one_flag":
+            ok = int(ln[3]) == fl
+        else:
+            ok = int(ln[1]) == fl and int(ln[3]) == fl
+        return [("read",)] if ok else []
+
+    def _next_step(self):
+        self.step += 1
+        self.line = 0
+        self.pub = False
+        self.early = False
+
+    def fire(self, choice):
+        if choice[0] == "head":
+            self.f.head = self.step + 1
+            if self.pub:
+                self._next_step()
+            else:
+                self.early = True
+            return
+        k = self.step % self.f.N
+        own = self.f.half_owner[k, self.line]
+        if own[0] != self.step or own[1] != self.step:
+            raise ProtocolViolation(f"LL line {self.line} of step {self.step} accepted with halves "
+                                    f"from steps {own[0]}, {own[1]}")
+        g = (self.step - self.base) * self.f.L + self.line
+        ln = self.f.lines[k, self.line]
+        self.out[self.lo + 2 * g] = ln[0]
+        self.out[self.lo + 2 * g + 1] = ln[2]
+        self.line += 1
+        if self.line == self._lines_in(self.step):
+            if self.early:
+                self._next_step()
+            else:
+                self.pub = True
+
+    def state(self):
+        return (self.step, self.line, self.pub, self.early)
+
+
+# --------------------------------------------------------------------------
+# Zero copy
+# --------------------------------------------------------------------------
+
+@dataclass
+class DstHandle:
+    """What the receiver publishes through ptrExchange: its buffer and offset."""
+    buf: np.ndarray
+    offset: int
+    reads: int = 0
+
+
+class ZeroCopyChannel:
+    """head, tail and the ptrExchange word of one channel; the staging slots
+    exist (poisoned) but zero copy must never touch them."""
+
+    def __init__(self, nslots: int, slot_bytes: int, step0: int = 0, poison: int = 0xA5):
+        self.N = nslots
+        self.S = slot_bytes
+        self.head = step0
+        self.tail = step0
+        self.ptr_exchange: DstHandle | None = None
+        self.slots = np.full((nslots, slot_bytes), poison, np.uint8)
+        self.max_occupancy = 0
+
+    def check(self):
+        occ = self.tail - self.head
+        if occ < 0 or occ > self.N:
+            raise ProtocolViolation(f"zero-copy tail {self.tail} head {self.head} N {self.N}")
+        self.max_occupancy = max(self.max_occupancy, occ)
+
+    def state(self):
+        h = self.ptr_exchange
+        return (self.head, self.tail, None if h is None else (h.offset, h.reads))
+
+
+class ZeroCopyReceiver(Actor):
+    """wait ptrExchange empty -> publish {dst, lo} -> per chunk: wait tail, store head."""
+    WAIT_EMPTY, POST, WAIT, PUB, DONE = range(5)
+
+    def __init__(self, ch: ZeroCopyChannel, dst: np.ndarray, lo: int, hi: int):
+        self.c, self.dst, self.lo, self.hi = ch, dst, lo, hi
+        self.base = ch.head
+        self.nchunks = ceil_div(hi - lo, ch.S)
+        self.j = 0
+        self.phase = self.WAIT_EMPTY if self.nchunks else self.DONE
+        self.name = f"zc-recv[{lo}:{hi}]"
+
+    def done(self):
+        return self.phase == self.DONE
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT_EMPTY:
+            return [0] if self.c.ptr_exchange is None else []
+        if self.phase == self.WAIT:
+            return [0] if self.c.tail > self.base + self.j else []
+        return [0]
+
+    def fire(self, choice):
+        if self.phase == self.WAIT_EMPTY:
+            self.phase = self.POST
+        elif self.phase == self.POST:
+            self.c.ptr_exchange = DstHandle(self.dst, self.lo)
+            self.phase = self.WAIT
+        elif self.phase == self.WAIT:
+            self.phase = self.PUB
+        elif self.phase == self.PUB:
+            self.c.head = self.base + self.j + 1
+            self.j += 1
+            self.phase = self.WAIT if self.j < self.nchunks else self.DONE
+
+    def state(self):
+        return (self.j, self.phase)
+
+
+class ZeroCopySender(Actor):
+    """wait ptrExchange -> per chunk: wait credit, write src chunk into the
+    published buffer, store tail -> wait final head -> empty ptrExchange.
+    `fault`: "no_clear" (leave ptrExchange set)."""
+    WAIT_PTR, WAIT, COPY, PUB, WAIT_FINAL, CLEAR, DONE = range(7)
+
+    def __init__(self, ch: ZeroCopyChannel, src: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.c, self.src, self.lo, self.hi = ch, src, lo, hi
+        self.base = ch.tail
+        self.nchunks = ceil_div(hi - lo, ch.S)
+        self.j = 0
+        self.h: DstHandle | None = None
+        self.phase = self.WAIT_PTR if self.nchunks else self.DONE
+        self.fault = fault
+        self.name = f"zc-send[{lo}:{hi}]"
+
+    def done(self):
+        return self.phase == self.DONE
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT_PTR:
+            return [0] if self.c.ptr_exchange is not None else []
+        if self.phase == self.WAIT:
+            return [0] if self.base + self.j < self.c.head + self.c.N else []
+        if self.phase == self.WAIT_FINAL:
+            return [0] if self.c.head == self.base + self.nchunks else []
+        return [0]
+
+    def fire(self, choice):
+        if self.phase == self.WAIT_PTR:
+            self.h = self.c.ptr_exchange
+            self.h.reads += 1
+            if self.h.reads != 1:
+                raise ProtocolViolation("ptrExchange value consumed twice")
+            self.phase = self.WAIT
+        elif self.phase == self.WAIT:
+            self.phase = self.COPY
+        elif self.phase == self.COPY:
+            off = self.j * self.c.S
+            n = min(self.hi - self.lo - off, self.c.S)
+            self.h.buf[self.h.offset + off:self.h.offset + off + n] = self.src[self.lo + off:self.lo + off + n]
+            self.phase = self.PUB
+        elif self.phase == self.PUB:
+            self.c.tail = self.base + self.j + 1
+            self.j += 1
+            self.phase = self.WAIT if self.j < self.nchunks else self.WAIT_FINAL
+        elif self.phase == self.WAIT_FINAL:
+            self.phase = self.CLEAR
+        elif self.phase == self.CLEAR:
+            if self.fault != "no_clear":
+                self.c.ptr_exchange = None
+            self.phase = self.DONE
+
+    def state(self):
+        return (self.j, self.phase)
+
+
+# --------------------------------------------------------------------------
+# Schedulers
+# --------------------------------------------------------------------------
+
+class System:
+    """Endpoints plus the shared objects whose invariants are checked."""
+
+    def __init__(self, actors: list[Actor], shared: list, buffers: list[np.ndarray] = ()):
+        self.actors = list(actors)
+        self.shared = list(shared)
+        self.buffers = list(buffers)
+
+    def options(self):
+        return [(i, c) for i, a in enumerate(self.actors) for c in a.choices()]
+
+    def all_done(self):
+        return all(a.done() for a in self.actors)
+
+    def check(self):
+        for s in self.shared:
+            s.check()
+
+    def key(self):
+        return (tuple(a.state() for a in self.actors), tuple(s.state() for s in self.shared),
+                tuple(b.tobytes() for b in self.buffers))
+
+
+def run(system: System, seed: int = 0, max_events: int | None = None) -> int:
+    """Fire random enabled events (numpy default_rng(seed)) until every
+    endpoint is done.  Returns the number of events fired."""
+    rng = np.random.default_rng(seed)
+    n = 0
+    while True:
+        opts = system.options()
+        if not opts:
+            if system.all_done():
+                return n
+            raise Deadlock("stuck: " + ", ".join(a.name for a in system.actors if not a.done()))
+        i, c = opts[int(rng.integers(len(opts)))]
+        system.actors[i].fire(c)
+        system.check()
+        n += 1
+        if max_events is not None and n >= max_events:
+            raise Deadlock(f"no completion within {max_events} events")
+
+
+def explore(make_system, final_check, limit: int = 2_000_000) -> int:
+    """Visit every state reachable by any interleaving of the endpoints'
+    events (depth first, states deduplicated).  Checks the invariants in
+    every state and `final_check(system)` in every terminal state; returns
+    the number of distinct states."""
+    start = make_system()
+    start.check()
+    stack = [start]
+    seen = set()
+    while stack:
+        s = stack.pop()
+        k = s.key()
+        if k in seen:
+            continue
+        seen.add(k)
+        if len(seen) > limit:
+            raise RuntimeError("state space larger than limit")
+        opts = s.options()
+        if not opts:
+            if not s.all_done():
+                raise Deadlock("stuck state reached")
+            final_check(s)
+            continue
+        for (i, c) in opts:
+            t = copy.deepcopy(s)
+            t.actors[i].fire(c)
+            t.check()
+            stack.append(t)
+    return len(seen)

@@ -1,0 +1,71 @@
+"""Whole transfers through the oracle's FIFO state machines (test infrastructure).
+
+Each function splits the buffer into channels by `partition.channel_byte_ranges`,
+builds one sender and one receiver per non-empty channel, runs them under a
+seeded random interleaving (`fifo.run`) and returns the destination with the
+FIFO objects, which can be passed back in to continue their step counters in
+a following transfer (the counters are monotonic across operations).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .fifo import (LLFifo, LLReceiver, LLSender, SimpleFifo, SimpleReceiver, SimpleSender, System,
+                   ZeroCopyChannel, ZeroCopyReceiver, ZeroCopySender, run)
+from .partition import channel_byte_ranges
+from .ring import ring_system
+
+
+def simple_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: int, seed: int = 0,
+                    fifos: list[SimpleFifo] | None = None):
+    """SIMPLE copy of the byte buffer `src`; returns (dst, fifos, events)."""
+    src = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
+    dst = np.zeros_like(src)
+    if fifos is None:
+        fifos = [SimpleFifo(nslots, slot_bytes) for _ in range(nchannels)]
+    actors = []
+    for f, (lo, hi) in zip(fifos, channel_byte_ranges(len(src), nchannels)):
+        if hi > lo:
+            actors += [SimpleSender(f, src, lo, hi), SimpleReceiver(f, dst, lo, hi)]
+    ev = run(System(actors, fifos, [dst]), seed=seed)
+    return dst, fifos, ev
+
+
+def ll_transfer(words: np.ndarray, nchannels: int, nslots: int, slot_bytes: int, seed: int = 0,
+                fifos: list[LLFifo] | None = None, window: int = 2):
+    """LL copy of the uint32 buffer `words` (even count); returns (out, fifos, events)."""
+    words = np.ascontiguousarray(words, dtype=np.uint32).reshape(-1)
+    if len(words) % 2:
+        raise ValueError("LL moves whole 8-byte lines")
+    out = np.zeros_like(words)
+    if fifos is None:
+        fifos = [LLFifo(nslots, slot_bytes) for _ in range(nchannels)]
+    actors = []
+    for f, (lo, hi) in zip(fifos, channel_byte_ranges(4 * len(words), nchannels)):
+        if hi > lo:
+            actors += [LLSender(f, words, lo // 4, hi // 4, window=window), LLReceiver(f, out, lo // 4, hi // 4)]
+    ev = run(System(actors, fifos, [out]), seed=seed)
+    return out, fifos, ev
+
+
+def zero_copy_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: int, seed: int = 0,
+                       chans: list[ZeroCopyChannel] | None = None):
+    """Zero-copy transfer of the byte buffer `src`; returns (dst, channels, events)."""
+    src = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
+    dst = np.zeros_like(src)
+    if chans is None:
+        chans = [ZeroCopyChannel(nslots, slot_bytes) for _ in range(nchannels)]
+    actors = []
+    for c, (lo, hi) in zip(chans, channel_byte_ranges(len(src), nchannels)):
+        if hi > lo:
+            actors += [ZeroCopySender(c, src, lo, hi), ZeroCopyReceiver(c, dst, lo, hi)]
+    ev = run(System(actors, chans, [dst]), seed=seed)
+    return dst, chans, ev
+
+
+def ring_allreduce(inputs: list[np.ndarray], nchannels: int, nslots: int, slot_bytes: int, seed: int = 0):
+    """Ring allreduce through per-rank FIFOs; returns (outputs, events)."""
+    outs = [np.zeros_like(x) for x in inputs]
+    sysm = ring_system(inputs, outs, nchannels, nslots, slot_bytes)
+    ev = run(sysm, seed=seed)
+    return outs, ev
