@@ -1,0 +1,537 @@
+// Host side of the C ABI declared in include/xp.h: argument checks, FIFO
+// memory (allocated once at create, as the channel buffers of "RDMA and
+// GPUDirect" §7.2), and one cluster launch per operation.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "xp_internal.h"
+
+namespace xp {
+void* p2p_kernel_ptr(bool zero_copy);
+void* ll_kernel_ptr();
+void* ll_pingpong_kernel_ptr();
+void* ring_kernel_ptr(int dtype);
+}  // namespace xp
+
+using xp::DevStatus;
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::mutex g_mu;
+int* g_abort_host = nullptr;
+int* g_abort_dev = nullptr;
+
+xp_status fail(xp_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define XP_CUDA(call)                                                                     \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess) return fail(XP_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+xp_status ensure_abort_word() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_abort_host) return XP_OK;
+  int* h = nullptr;
+  XP_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&h), 64, cudaHostAllocMapped | cudaHostAllocPortable));
+  memset(h, 0, 64);
+  int* d = nullptr;
+  cudaError_t e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&d), h, 0);
+  if (e != cudaSuccess) {
+    cudaFreeHost(h);
+    return fail(XP_ERR_CUDA, "cudaHostGetDevicePointer: %s", cudaGetErrorString(e));
+  }
+  g_abort_host = h;
+  g_abort_dev = d;
+  return XP_OK;
+}
+
+// One allocation holding control blocks and slots, in HBM or mapped host memory.
+struct Mem {
+  char* host = nullptr;   // host view (mapped placement only)
+  char* dev = nullptr;    // device view
+  size_t bytes = 0;
+  xp_placement place = XP_PLACE_DEVICE;
+};
+
+xp_status mem_alloc(Mem& m, size_t bytes, xp_placement place) {
+  m.bytes = bytes;
+  m.place = place;
+  if (place == XP_PLACE_DEVICE) {
+    XP_CUDA(cudaMalloc(reinterpret_cast<void**>(&m.dev), bytes));
+  } else {
+    XP_CUDA(cudaHostAlloc(reinterpret_cast<void**>(&m.host), bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+    cudaError_t e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&m.dev), m.host, 0);
+    if (e != cudaSuccess) {
+      cudaFreeHost(m.host);
+      m.host = nullptr;
+      return fail(XP_ERR_CUDA, "cudaHostGetDevicePointer: %s", cudaGetErrorString(e));
+    }
+  }
+  return XP_OK;
+}
+
+void mem_free(Mem& m) {
+  if (m.place == XP_PLACE_DEVICE) {
+    if (m.dev) cudaFree(m.dev);
+  } else if (m.host) {
+    cudaFreeHost(m.host);
+  }
+  m.host = m.dev = nullptr;
+}
+
+// Zero the whole region, then set every size word of `nfifos` control
+// blocks to -1.
+xp_status mem_init(Mem& m, int nfifos) {
+  const size_t ctl_bytes = (size_t)nfifos * xp::kCtlBytes;
+  std::vector<char> img(ctl_bytes, 0);
+  for (int f = 0; f < nfifos; ++f) {
+    long long* sz = reinterpret_cast<long long*>(img.data() + (size_t)f * xp::kCtlBytes + xp::kSizeOff);
+    for (int k = 0; k < xp::kMaxSlots; ++k) sz[k] = -1;
+  }
+  if (m.place == XP_PLACE_DEVICE) {
+    XP_CUDA(cudaMemset(m.dev, 0, m.bytes));
+    XP_CUDA(cudaMemcpy(m.dev, img.data(), ctl_bytes, cudaMemcpyHostToDevice));
+  } else {
+    memset(m.host, 0, m.bytes);
+    memcpy(m.host, img.data(), ctl_bytes);
+  }
+  return XP_OK;
+}
+
+struct Common {
+  int device = 0;
+  DevStatus* status = nullptr;   // device memory
+  cudaEvent_t done = nullptr;
+  cudaStream_t query = nullptr;
+  bool used = false;
+};
+
+xp_status common_init(Common& c) {
+  XP_CUDA(cudaGetDevice(&c.device));
+  XP_CUDA(cudaMalloc(reinterpret_cast<void**>(&c.status), sizeof(DevStatus)));
+  XP_CUDA(cudaMemset(c.status, 0, sizeof(DevStatus)));
+  XP_CUDA(cudaEventCreateWithFlags(&c.done, cudaEventDisableTiming));
+  XP_CUDA(cudaStreamCreateWithFlags(&c.query, cudaStreamNonBlocking));
+  return XP_OK;
+}
+
+void common_free(Common& c) {
+  if (c.done) cudaEventSynchronize(c.done);
+  if (c.status) cudaFree(c.status);
+  if (c.done) cudaEventDestroy(c.done);
+  if (c.query) cudaStreamDestroy(c.query);
+  c = Common();
+}
+
+xp_status check_device(const Common& c) {
+  int d = -1;
+  XP_CUDA(cudaGetDevice(&d));
+  if (d != c.device) return fail(XP_ERR_INVALID, "current device %d is not the object's device %d", d, c.device);
+  return XP_OK;
+}
+
+xp_status read_status(Common& c, int sync, xp_report* rep) {
+  if (sync && c.used) XP_CUDA(cudaEventSynchronize(c.done));
+  DevStatus h;
+  XP_CUDA(cudaMemcpyAsync(&h, c.status, sizeof h, cudaMemcpyDeviceToHost, c.query));
+  XP_CUDA(cudaStreamSynchronize(c.query));
+  if (rep) {
+    rep->code = h.code;
+    rep->channel = h.code ? h.channel : -1;
+    rep->where = h.where;
+    rep->reserved = 0;
+    rep->observed = h.observed;
+    rep->expected = h.expected;
+    rep->max_occupancy = h.max_occupancy;
+    rep->reserved2 = 0;
+  }
+  if (h.code < 0 || h.code > XP_ERR_INTERNAL) return XP_ERR_INTERNAL;
+  return static_cast<xp_status>(h.code);
+}
+
+// Cluster co-residency: every cluster of the launch must fit on the GPU.
+std::map<std::tuple<const void*, int, int>, int> g_fits;
+
+xp_status launch(const void* kernel, int grid, int block, int csize, void* params, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = csize;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(kernel, csize, block);
+    auto it = g_fits.find(key);
+    if (it == g_fits.end()) {
+      if (csize > 8) XP_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+      int n = 0;
+      XP_CUDA(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
+      it = g_fits.emplace(key, n).first;
+    }
+    if (it->second < 1)
+      return fail(XP_ERR_INVALID, "a cluster of %d CTAs x %d threads cannot be resident on this GPU", csize, block);
+  }
+  void* args[] = {params};
+  XP_CUDA(cudaLaunchKernelExC(&cfg, kernel, args));
+  return XP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct xp_fifo {
+  Common cm;
+  int C = 0, N = 0;
+  size_t S = 0;
+  xp_proto proto = XP_PROTO_SIMPLE;
+  xp_placement place = XP_PLACE_DEVICE;
+  int lanes = 1;
+  Mem mem;
+  char* ctl = nullptr;     // device view
+  char* slots = nullptr;   // device view
+  size_t ctl_region = 0;
+  size_t ch_stride = 0;
+};
+
+struct xp_ring {
+  Common cm;
+  int P = 0, C = 0, N = 0;
+  size_t S = 0;
+  xp_placement place = XP_PLACE_DEVICE;
+  int lanes = 1;
+  Mem mem;
+  char* ctl = nullptr;
+  char* slots = nullptr;
+  size_t ctl_region = 0;
+  size_t fifo_stride = 0;
+};
+
+extern "C" {
+
+int xp_version(void) { return 1; }
+
+const char* xp_last_error(void) { return g_err.c_str(); }
+
+const char* xp_status_string(xp_status s) {
+  switch (s) {
+    case XP_OK: return "ok";
+    case XP_ERR_INVALID: return "invalid argument";
+    case XP_ERR_CUDA: return "CUDA error";
+    case XP_ERR_TIMEOUT: return "device wait timed out";
+    case XP_ERR_BOUNDS: return "size word or occupancy out of bounds";
+    case XP_ERR_ABORTED: return "aborted";
+    case XP_ERR_INTERNAL: return "internal error";
+  }
+  return "unknown status";
+}
+
+xp_status xp_set_spin_timeout_ns(uint64_t ns) {
+  if (ns < 1000ull || ns > 60000000000ull) return fail(XP_ERR_INVALID, "timeout %llu ns out of range", (unsigned long long)ns);
+  g_timeout_ns = ns;
+  return XP_OK;
+}
+
+xp_status xp_abort(int value) {
+  xp_status s = ensure_abort_word();
+  if (s != XP_OK) return s;
+  *reinterpret_cast<volatile int*>(g_abort_host) = value ? 1 : 0;
+  return XP_OK;
+}
+
+xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto proto, xp_placement place,
+                         xp_fifo** out) {
+  if (!out) return fail(XP_ERR_INVALID, "out is NULL");
+  if (nchannels < 1 || nchannels > xp::kMaxChannels) return fail(XP_ERR_INVALID, "nchannels %d not in [1, 64]", nchannels);
+  if (nslots < 1 || nslots > xp::kMaxSlots) return fail(XP_ERR_INVALID, "nslots %d not in [1, 64]", nslots);
+  if (slot_bytes == 0 || slot_bytes % 16 || slot_bytes > (1ull << 31))
+    return fail(XP_ERR_INVALID, "slot_bytes %zu must be a non-zero multiple of 16, at most 2^31", slot_bytes);
+  if (proto != XP_PROTO_SIMPLE && proto != XP_PROTO_LL) return fail(XP_ERR_INVALID, "unknown protocol %d", (int)proto);
+  if (place != XP_PLACE_DEVICE && place != XP_PLACE_HOST_MAPPED) return fail(XP_ERR_INVALID, "unknown placement %d", (int)place);
+  if ((unsigned long long)nchannels * nslots * slot_bytes > (1ull << 40)) return fail(XP_ERR_INVALID, "FIFO larger than 2^40 bytes");
+  xp_status s = ensure_abort_word();
+  if (s != XP_OK) return s;
+  xp_fifo* f = new xp_fifo();
+  f->C = nchannels;
+  f->N = nslots;
+  f->S = slot_bytes;
+  f->proto = proto;
+  f->place = place;
+  f->ctl_region = round_up((size_t)nchannels * xp::kCtlBytes, 4096);
+  f->ch_stride = round_up((size_t)nslots * slot_bytes, 4096);
+  if ((s = common_init(f->cm)) != XP_OK || (s = mem_alloc(f->mem, f->ctl_region + nchannels * f->ch_stride, place)) != XP_OK ||
+      (s = mem_init(f->mem, nchannels)) != XP_OK) {
+    common_free(f->cm);
+    mem_free(f->mem);
+    delete f;
+    return s;
+  }
+  f->ctl = f->mem.dev;
+  f->slots = f->mem.dev + f->ctl_region;
+  *out = f;
+  return XP_OK;
+}
+
+xp_status xp_fifo_destroy(xp_fifo* f) {
+  if (!f) return XP_OK;
+  cudaDeviceSynchronize();
+  common_free(f->cm);
+  mem_free(f->mem);
+  delete f;
+  return XP_OK;
+}
+
+xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
+  if (lanes < 1 || lanes > 8) return fail(XP_ERR_INVALID, "lanes %d not in [1, 8]", lanes);
+  f->lanes = lanes;
+  return XP_OK;
+}
+
+xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out) {
+  if (!f || !out) return fail(XP_ERR_INVALID, "NULL argument");
+  if (channel < 0 || channel >= f->C) return fail(XP_ERR_INVALID, "channel %d out of range", channel);
+  out->ctl = f->ctl + (size_t)channel * xp::kCtlBytes;
+  out->slots = f->slots + (size_t)channel * f->ch_stride;
+  out->slot_stride = f->S;
+  out->nslots = f->N;
+  out->proto = f->proto;
+  out->placement = f->place;
+  out->lanes = f->lanes;
+  return XP_OK;
+}
+
+static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream, bool zero_copy) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  if (bytes == 0) return XP_OK;
+  if (!src || !dst) return fail(XP_ERR_INVALID, "src or dst is NULL");
+  if (!aligned16(src) || !aligned16(dst)) return fail(XP_ERR_INVALID, "src and dst must be 16-byte aligned");
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  if (s0 < d0 + bytes && d0 < s0 + bytes) return fail(XP_ERR_INVALID, "src and dst overlap");
+  if (zero_copy && f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "zero copy needs a SIMPLE FIFO");
+  if (f->proto == XP_PROTO_LL && bytes % 8) return fail(XP_ERR_INVALID, "LL moves whole 8-byte lines: bytes %% 8 != 0");
+  xp_status s = check_device(f->cm);
+  if (s != XP_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  xp::P2pParams p = {};
+  p.ctl = f->ctl;
+  p.slots = f->slots;
+  p.ch_stride = f->ch_stride;
+  p.src = static_cast<const char*>(src);
+  p.dst = static_cast<char*>(dst);
+  p.nbytes = bytes;
+  p.nchannels = f->C;
+  p.nslots = f->N;
+  p.slot_bytes = (unsigned)f->S;
+  p.status = f->cm.status;
+  p.abort_word = g_abort_dev;
+  p.timeout_ns = g_timeout_ns.load();
+  const void* kernel;
+  int csize, block;
+  if (f->proto == XP_PROTO_LL) {
+    kernel = xp::ll_kernel_ptr();
+    p.lanes = 1;
+    csize = 2;
+    block = xp::kLLThreads;
+  } else {
+    kernel = xp::p2p_kernel_ptr(zero_copy);
+    p.lanes = f->lanes;
+    csize = zero_copy ? f->lanes + 1 : 2 * f->lanes;
+    block = xp::kP2pThreads;
+  }
+  p.csize = csize;
+  XP_CUDA(cudaMemsetAsync(f->cm.status, 0, xp::kStatusClearBytes, st));
+  if ((s = launch(kernel, f->C * csize, block, csize, &p, st)) != XP_OK) return s;
+  XP_CUDA(cudaEventRecord(f->cm.done, st));
+  f->cm.used = true;
+  return XP_OK;
+}
+
+xp_status xp_send_recv(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream) {
+  return p2p_op(f, src, dst, bytes, stream, false);
+}
+
+xp_status xp_send_recv_zero_copy(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream) {
+  return p2p_op(f, src, dst, bytes, stream, true);
+}
+
+xp_status xp_fifo_status(xp_fifo* f, int sync, xp_report* report) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  return read_status(f->cm, sync, report);
+}
+
+xp_status xp_fifo_reset(xp_fifo* f) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  if (f->cm.used) XP_CUDA(cudaEventSynchronize(f->cm.done));
+  XP_CUDA(cudaMemset(f->cm.status, 0, sizeof(DevStatus)));
+  return mem_init(f->mem, f->C);
+}
+
+xp_status xp_ll_pingpong(xp_fifo* ab, xp_fifo* ba, int iters, uint64_t* elapsed_ns, xp_stream_t stream) {
+  if (!ab || !ba || !elapsed_ns) return fail(XP_ERR_INVALID, "NULL argument");
+  if (ab == ba) return fail(XP_ERR_INVALID, "ping-pong needs two FIFOs");
+  if (ab->proto != XP_PROTO_LL || ba->proto != XP_PROTO_LL) return fail(XP_ERR_INVALID, "ping-pong needs LL FIFOs");
+  if (iters < 1 || iters > 10000000) return fail(XP_ERR_INVALID, "iters %d not in [1, 1e7]", iters);
+  xp_status s = check_device(ab->cm);
+  if (s != XP_OK) return s;
+  if ((s = check_device(ba->cm)) != XP_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  xp::PingParams p = {};
+  p.ctl_ab = ab->ctl;
+  p.slots_ab = ab->slots;
+  p.ctl_ba = ba->ctl;
+  p.slots_ba = ba->slots;
+  p.nslots_ab = ab->N;
+  p.nslots_ba = ba->N;
+  p.slot_bytes_ab = (unsigned)ab->S;
+  p.slot_bytes_ba = (unsigned)ba->S;
+  p.iters = iters;
+  p.elapsed = reinterpret_cast<unsigned long long*>(&ab->cm.status->pad1[0]);
+  p.status = ab->cm.status;
+  p.abort_word = g_abort_dev;
+  p.timeout_ns = g_timeout_ns.load();
+  XP_CUDA(cudaMemsetAsync(ab->cm.status, 0, xp::kStatusClearBytes, st));
+  if ((s = launch(xp::ll_pingpong_kernel_ptr(), 2, 32, 2, &p, st)) != XP_OK) return s;
+  XP_CUDA(cudaEventRecord(ab->cm.done, st));
+  XP_CUDA(cudaEventRecord(ba->cm.done, st));
+  ab->cm.used = ba->cm.used = true;
+  XP_CUDA(cudaEventSynchronize(ab->cm.done));
+  DevStatus h;
+  XP_CUDA(cudaMemcpy(&h, ab->cm.status, sizeof h, cudaMemcpyDeviceToHost));
+  if (h.code != XP_OK) return static_cast<xp_status>(h.code);
+  *elapsed_ns = h.pad1[0];
+  return XP_OK;
+}
+
+xp_status xp_ring_create(int nranks, int nchannels, int nslots, size_t slot_bytes, xp_placement place, xp_ring** out) {
+  if (!out) return fail(XP_ERR_INVALID, "out is NULL");
+  if (nranks < 2 || nranks > xp::kMaxRanks) return fail(XP_ERR_INVALID, "nranks %d not in [2, 16]", nranks);
+  if (nchannels < 1 || nchannels > xp::kMaxChannels) return fail(XP_ERR_INVALID, "nchannels %d not in [1, 64]", nchannels);
+  if (nslots < 2 || nslots > xp::kMaxSlots) return fail(XP_ERR_INVALID, "the ring needs 2 <= nslots <= 64, got %d", nslots);
+  if (slot_bytes == 0 || slot_bytes % 16 || slot_bytes > (1ull << 31))
+    return fail(XP_ERR_INVALID, "slot_bytes %zu must be a non-zero multiple of 16, at most 2^31", slot_bytes);
+  if (place != XP_PLACE_DEVICE && place != XP_PLACE_HOST_MAPPED) return fail(XP_ERR_INVALID, "unknown placement %d", (int)place);
+  if ((unsigned long long)nranks * nchannels * nslots * slot_bytes > (1ull << 40)) return fail(XP_ERR_INVALID, "FIFOs larger than 2^40 bytes");
+  xp_status s = ensure_abort_word();
+  if (s != XP_OK) return s;
+  xp_ring* r = new xp_ring();
+  r->P = nranks;
+  r->C = nchannels;
+  r->N = nslots;
+  r->S = slot_bytes;
+  r->place = place;
+  const int nf = nranks * nchannels;
+  r->ctl_region = round_up((size_t)nf * xp::kCtlBytes, 4096);
+  r->fifo_stride = round_up((size_t)nslots * slot_bytes, 4096);
+  if ((s = common_init(r->cm)) != XP_OK || (s = mem_alloc(r->mem, r->ctl_region + nf * r->fifo_stride, place)) != XP_OK ||
+      (s = mem_init(r->mem, nf)) != XP_OK) {
+    common_free(r->cm);
+    mem_free(r->mem);
+    delete r;
+    return s;
+  }
+  r->ctl = r->mem.dev;
+  r->slots = r->mem.dev + r->ctl_region;
+  *out = r;
+  return XP_OK;
+}
+
+xp_status xp_ring_destroy(xp_ring* r) {
+  if (!r) return XP_OK;
+  cudaDeviceSynchronize();
+  common_free(r->cm);
+  mem_free(r->mem);
+  delete r;
+  return XP_OK;
+}
+
+xp_status xp_ring_set_lanes(xp_ring* r, int lanes) {
+  if (!r) return fail(XP_ERR_INVALID, "ring is NULL");
+  if (lanes < 1 || r->P * lanes > xp::kMaxCluster) return fail(XP_ERR_INVALID, "nranks * lanes must be <= 16");
+  r->lanes = lanes;
+  return XP_OK;
+}
+
+xp_status xp_ring_allreduce_virtual(xp_ring* r, const void* const* send_bufs, void* const* recv_bufs, size_t count,
+                                    xp_dtype dt, xp_stream_t stream) {
+  if (!r) return fail(XP_ERR_INVALID, "ring is NULL");
+  if (dt != XP_F32 && dt != XP_I32) return fail(XP_ERR_INVALID, "the ring reduces XP_F32 or XP_I32 only");
+  if (count == 0) return XP_OK;
+  if (!send_bufs || !recv_bufs) return fail(XP_ERR_INVALID, "buffer arrays are NULL");
+  if (count > (1ull << 38)) return fail(XP_ERR_INVALID, "count too large");
+  for (int i = 0; i < r->P; ++i) {
+    if (!send_bufs[i] || !recv_bufs[i]) return fail(XP_ERR_INVALID, "rank %d buffer is NULL", i);
+    if (!aligned16(send_bufs[i]) || !aligned16(recv_bufs[i])) return fail(XP_ERR_INVALID, "rank %d buffer not 16-byte aligned", i);
+  }
+  xp_status s = check_device(r->cm);
+  if (s != XP_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  xp::RingParams p = {};
+  p.ctl = r->ctl;
+  p.slots = r->slots;
+  p.fifo_stride = r->fifo_stride;
+  for (int i = 0; i < r->P; ++i) {
+    p.send[i] = static_cast<const char*>(send_bufs[i]);
+    p.recv[i] = static_cast<char*>(recv_bufs[i]);
+  }
+  p.count = count;
+  p.nranks = r->P;
+  p.nchannels = r->C;
+  p.nslots = r->N;
+  p.lanes = r->lanes;
+  p.dtype = dt;
+  p.slot_bytes = (unsigned)r->S;
+  p.status = r->cm.status;
+  p.abort_word = g_abort_dev;
+  p.timeout_ns = g_timeout_ns.load();
+  const int csize = r->P * r->lanes;
+  XP_CUDA(cudaMemsetAsync(r->cm.status, 0, xp::kStatusClearBytes, st));
+  if ((s = launch(xp::ring_kernel_ptr(dt), r->C * csize, xp::kRingThreads, csize, &p, st)) != XP_OK) return s;
+  XP_CUDA(cudaEventRecord(r->cm.done, st));
+  r->cm.used = true;
+  return XP_OK;
+}
+
+xp_status xp_ring_status(xp_ring* r, int sync, xp_report* report) {
+  if (!r) return fail(XP_ERR_INVALID, "ring is NULL");
+  return read_status(r->cm, sync, report);
+}
+
+xp_status xp_ring_reset(xp_ring* r) {
+  if (!r) return fail(XP_ERR_INVALID, "ring is NULL");
+  if (r->cm.used) XP_CUDA(cudaEventSynchronize(r->cm.done));
+  XP_CUDA(cudaMemset(r->cm.status, 0, sizeof(DevStatus)));
+  return mem_init(r->mem, r->P * r->C);
+}
+
+}  // extern "C"

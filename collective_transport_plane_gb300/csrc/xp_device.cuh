@@ -1,0 +1,253 @@
+// Device primitives of the FIFO data plane: ordered counter access, bounded
+// waits, cluster mbarriers and warp-wide copies.  sm_103a only.
+#pragma once
+
+#include <cstdint>
+
+#include "xp_internal.h"
+
+namespace xp {
+
+typedef unsigned long long u64;
+
+// ---- ordered accesses on the control words (.gpu scope: every endpoint is
+// ---- a thread of this GPU, also when the word lives in mapped host memory)
+__device__ __forceinline__ u64 ld_acquire(const u64* p) {
+  u64 v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ u64 ld_relaxed(const u64* p) {
+  u64 v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(u64* p, u64 v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed(u64* p, u64 v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ u64 globaltimer() {
+  u64 t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- LL line: two 8-byte halves {data, flag}, each a single-copy-atomic u64
+__device__ __forceinline__ void ll_store(void* p, u64 a, u64 b) {
+  asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void ll_load(const void* p, u64& a, u64& b) {
+  asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+// ---- cluster and mbarrier helpers
+__device__ __forceinline__ unsigned cluster_ctarank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_init(uint32_t saddr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Arrive (release, cluster scope) on an mbarrier in any CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_saddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_saddr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t saddr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// ---- error reporting and bounded waits
+struct WaitCtx {
+  DevStatus* st;
+  const volatile int* abort_word;
+  u64 timeout_ns;
+  int channel;
+};
+
+__device__ __forceinline__ void report(const WaitCtx& w, int code, int where, u64 observed, u64 expected) {
+  if (atomicCAS(&w.st->code, 0, code) == 0) {
+    w.st->channel = w.channel;
+    w.st->where = where;
+    w.st->observed = observed;
+    w.st->expected = expected;
+  }
+  atomicExch(&w.st->sticky, 1);
+  atomicExch(&w.st->abort, 1);
+}
+
+__device__ __forceinline__ bool op_aborted(const WaitCtx& w) {
+  if (*reinterpret_cast<volatile int*>(&w.st->abort)) return true;
+  if (w.abort_word && *w.abort_word) {
+    report(w, XP_ERR_ABORTED, XP_WAIT_NONE, 0, 0);
+    return true;
+  }
+  return false;
+}
+
+// Poll `*p` (acquire) until it is >= target.  One thread.  Gives up on the
+// operation's abort flag, the host abort word, or after timeout_ns.
+static __device__ __noinline__ bool wait_geq(const u64* p, u64 target, u64& cache, const WaitCtx& w, int where) {
+  if (cache >= target) return true;
+  u64 start = 0;
+  unsigned it = 0;
+  for (;;) {
+    u64 v = ld_acquire(p);
+    if (v >= target) {
+      cache = v;
+      return true;
+    }
+    if ((++it & 127u) == 0) {
+      if (op_aborted(w)) return false;
+      u64 now = globaltimer();
+      if (start == 0) {
+        start = now;
+      } else if (now - start > w.timeout_ns) {
+        report(w, XP_ERR_TIMEOUT, where, v, target);
+        return false;
+      }
+    }
+  }
+}
+
+// Same for a word that must become zero (mode 0) or non-zero (mode 1).
+static __device__ __noinline__ bool wait_word(const u64* p, int nonzero, u64& value, const WaitCtx& w, int where) {
+  u64 start = 0;
+  unsigned it = 0;
+  for (;;) {
+    u64 v = ld_acquire(p);
+    if ((v != 0) == (nonzero != 0)) {
+      value = v;
+      return true;
+    }
+    if ((++it & 127u) == 0) {
+      if (op_aborted(w)) return false;
+      u64 now = globaltimer();
+      if (start == 0) {
+        start = now;
+      } else if (now - start > w.timeout_ns) {
+        report(w, XP_ERR_TIMEOUT, where, v, nonzero ? 1 : 0);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-wide wait: lane 0 polls with acquire, __syncwarp orders the other
+// lanes' later accesses after it.
+__device__ __forceinline__ bool warp_wait_geq(const u64* p, u64 target, u64& cache, const WaitCtx& w, int where) {
+  if (cache >= target) return true;   // warp-uniform: every lane holds the same cache
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  u64 c = cache;
+  if (lane == 0) ok = wait_geq(p, target, c, w, where);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  cache = __shfl_sync(0xffffffffu, c, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+static __device__ __noinline__ bool mbar_wait(uint32_t saddr, uint32_t parity, const WaitCtx& w, int where, u64 step) {
+  u64 start = 0;
+  unsigned it = 0;
+  while (!mbar_try_wait(saddr, parity)) {
+    if ((++it & 15u) == 0) {
+      if (op_aborted(w)) return false;
+      u64 now = globaltimer();
+      if (start == 0) {
+        start = now;
+      } else if (now - start > w.timeout_ns) {
+        report(w, XP_ERR_TIMEOUT, where, step, step + 1);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// ---- copies: one warp moves [0, nbytes) with 16-byte vectors (src, dst
+// ---- 16-byte aligned; a ragged tail of < 16 bytes is moved bytewise)
+enum { LD_STREAM = 0, LD_L2 = 1 };
+enum { ST_STREAM = 0, ST_L2 = 1 };
+
+template <int LD>
+__device__ __forceinline__ uint4 vload(const uint4* p) {
+  if (LD == LD_STREAM) return __ldcs(p);
+  return __ldcg(p);
+}
+template <int ST>
+__device__ __forceinline__ void vstore(uint4* p, uint4 v) {
+  if (ST == ST_STREAM)
+    __stcs(p, v);
+  else
+    __stcg(p, v);
+}
+
+template <int LD, int ST>
+__device__ __forceinline__ void warp_copy(const char* src, char* dst, u64 nbytes) {
+  const int lane = threadIdx.x & 31;
+  const u64 nvec = nbytes >> 4;
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  u64 i = lane;
+  for (; i + 96 < nvec; i += 128) {
+    uint4 a = vload<LD>(s + i);
+    uint4 b = vload<LD>(s + i + 32);
+    uint4 c = vload<LD>(s + i + 64);
+    uint4 e = vload<LD>(s + i + 96);
+    vstore<ST>(d + i, a);
+    vstore<ST>(d + i + 32, b);
+    vstore<ST>(d + i + 64, c);
+    vstore<ST>(d + i + 96, e);
+  }
+  for (; i < nvec; i += 32) vstore<ST>(d + i, vload<LD>(s + i));
+  const u64 done = nvec << 4;
+  if (done + lane < nbytes) dst[done + lane] = __ldcg(src + done + lane);
+}
+
+// Balanced split of `nbytes` (16-byte vectors, the last possibly short) into
+// `parts` contiguous pieces; returns piece `i` as [*b0, *b1).
+__device__ __forceinline__ void piece(u64 nbytes, u64 parts, u64 i, u64* b0, u64* b1) {
+  const u64 nvec = (nbytes + 15) >> 4;
+  const u64 v0 = (nvec * i) / parts;
+  const u64 v1 = (nvec * (i + 1)) / parts;
+  *b0 = v0 << 4;
+  *b1 = (v1 << 4) < nbytes ? (v1 << 4) : nbytes;
+  if (*b0 > *b1) *b0 = *b1;
+}
+
+// Channel c's byte range [lo, hi): q = round_up(ceil(n / C), 16).
+__device__ __forceinline__ void channel_range(u64 n, int C, int c, u64* lo, u64* hi) {
+  u64 q = (n + C - 1) / C;
+  q = (q + 15) & ~15ull;
+  u64 a = q * c, b = q * (c + 1);
+  *lo = a < n ? a : n;
+  *hi = b < n ? b : n;
+}
+
+}  // namespace xp

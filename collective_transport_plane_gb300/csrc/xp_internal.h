@@ -1,0 +1,100 @@
+// Definitions shared by the host library and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/xp.h"
+
+namespace xp {
+
+constexpr int kMaxSlots = 64;
+constexpr int kMaxChannels = 64;
+constexpr int kMaxRanks = 16;
+constexpr int kMaxCluster = 16;
+
+// Per-channel control block: every word the two sides write sits on its own
+// 128-byte line, so the producer's tail stores and the consumer's head stores
+// never share a line (and neither shares one with the size words).
+constexpr int kCtlBytes = 1024;
+constexpr int kTailOff = 0;     // producer cursor (lives with the receiver)
+constexpr int kHeadOff = 128;   // consumer cursor / credit (lives with the sender)
+constexpr int kPtrxOff = 256;   // ptrExchange: receiver's destination for zero copy
+constexpr int kBaseOff = 384;   // first step of the next operation (device-side epoch)
+constexpr int kSizeOff = 512;   // int64 size word per slot, -1 = never written
+
+constexpr int kCopyWarps = 16;                  // data-moving warps per CTA
+constexpr int kP2pThreads = 32 * (kCopyWarps + 1);   // + 1 publisher warp
+constexpr int kRingThreads = 32 * (kCopyWarps + 2);  // + tail and head publishers
+constexpr int kLLThreads = 32 * (kCopyWarps + 1);
+
+// Device-side status of one operation (device memory).  The first 64 bytes
+// are cleared before every operation; `sticky` survives until a reset.
+struct DevStatus {
+  int code;
+  int channel;
+  int where;
+  int abort;                      // set by the first failing wait: the others stop early
+  unsigned long long observed;
+  unsigned long long expected;
+  unsigned int max_occupancy;
+  int pad0;
+  unsigned long long pad1[3];
+  int sticky;                     // +64
+  int pad2[15];
+};
+static_assert(sizeof(DevStatus) == 128, "status block layout");
+constexpr int kStatusClearBytes = 64;
+
+struct P2pParams {
+  char* ctl;                      // nchannels control blocks
+  char* slots;                    // channel c's slot k at slots + c*ch_stride + k*slot_bytes
+  unsigned long long ch_stride;
+  const char* src;
+  char* dst;
+  unsigned long long nbytes;
+  int nchannels;
+  int nslots;
+  int lanes;                      // CTAs per side per channel
+  int csize;                      // cluster size
+  unsigned int slot_bytes;
+  DevStatus* status;
+  const volatile int* abort_word; // mapped host memory
+  unsigned long long timeout_ns;
+};
+
+struct PingParams {
+  char* ctl_ab;
+  char* slots_ab;
+  char* ctl_ba;
+  char* slots_ba;
+  int nslots_ab;
+  int nslots_ba;
+  unsigned int slot_bytes_ab;
+  unsigned int slot_bytes_ba;
+  int iters;
+  unsigned long long* elapsed;    // device word
+  DevStatus* status;
+  const volatile int* abort_word;
+  unsigned long long timeout_ns;
+};
+
+struct RingParams {
+  char* ctl;                      // FIFO (c, r) control block at ctl + (c*nranks + r)*kCtlBytes
+  char* slots;                    // its slots at slots + (c*nranks + r)*fifo_stride
+  unsigned long long fifo_stride;
+  const char* send[kMaxRanks];
+  char* recv[kMaxRanks];
+  unsigned long long count;
+  int nranks;
+  int nchannels;
+  int nslots;
+  int lanes;
+  int dtype;                      // XP_F32 or XP_I32
+  unsigned int slot_bytes;
+  DevStatus* status;
+  const volatile int* abort_word;
+  unsigned long long timeout_ns;
+};
+
+}  // namespace xp

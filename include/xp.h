@@ -1,0 +1,230 @@
+/*
+ * xp.h — C ABI of a single-GPU collective-transport data plane for GB300.
+ *
+ * A sender copies a user buffer, in slot-sized steps, into a bounded
+ * circular FIFO and publishes a tail counter; a receiver waits on tail,
+ * copies (or reduces) each slot into its destination and returns credit
+ * through a head counter.  Every endpoint is a group of CTAs on one GPU.
+ *
+ * Sources (page title, section):
+ *   [setup]    "NCCL transport setup" (gitcode.csdn.net): p2pRecvConnect wires
+ *              tail (receiver memory), head (sender memory), ptrExchange and
+ *              stepSize = buffSize / NCCL_STEPS; 具体说明 gives the ring
+ *              neighbours; shmTransport places buffers and tail in host memory
+ *              that the GPU reads directly; the receiver allocates the data
+ *              buffers and tail, the sender only head.
+ *   [transfer] "NCCL transport data transfer (二)" (cnnetsun.cn): p2pTransport
+ *              zero copy through ptrExchange, copy mode (slot, tail, head),
+ *              shmTransport normal mode.
+ *   [rdma]     "RDMA and GPUDirect" (arganzheng.life) §4.1: the LL protocols
+ *              put the flag in the data and the receiver polls memory; §7.2:
+ *              4 MB channel buffers allocated once at connection time.
+ *   [neuron]   "Intra-Node Transport (P2P)" (gh.evko.io) §4: POST/POLL on
+ *              head/tail is device-only, the host does nothing.
+ *
+ * Conventions for every call:
+ *   - Pointers named src/dst/send_bufs/recv_bufs are device pointers (or
+ *     device-accessible mapped host pointers) owned by the caller; they must
+ *     be 16-byte aligned and must stay valid until the operation completes
+ *     on its stream.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream); every
+ *     data-moving call is asynchronous on it and launches exactly one kernel
+ *     after a small cudaMemsetAsync of the operation's status block.
+ *   - Operations on one FIFO (or one ring) must be ordered: issue them on one
+ *     stream, or synchronise between them.  Step counters live on the device
+ *     and carry over from one operation to the next, so captured CUDA graphs
+ *     may be replayed.
+ *   - Argument errors return immediately (no launch).  A CUDA error from a
+ *     launch returns XP_ERR_CUDA (message in xp_last_error()).  Errors found
+ *     on the device (a wait that timed out, a size word or occupancy out of
+ *     bounds, an abort request) are reported by xp_fifo_status /
+ *     xp_ring_status; after one, the object refuses further work (its next
+ *     operations report XP_ERR_ABORTED) until xp_fifo_reset / xp_ring_reset.
+ *   - No call allocates memory except *_create; no call spins on the host
+ *     except the *_status calls with sync != 0 and *_destroy.
+ */
+#ifndef XP_H
+#define XP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Result codes, modelled on ncclResult_t ([setup]: ncclSuccess,
+ * ncclInvalidArgument, ncclInternalError). */
+typedef enum {
+  XP_OK = 0,
+  XP_ERR_INVALID = 1,   /* bad argument; nothing was launched            */
+  XP_ERR_CUDA = 2,      /* a CUDA call failed; see xp_last_error()       */
+  XP_ERR_TIMEOUT = 3,   /* a device wait exceeded the spin timeout       */
+  XP_ERR_BOUNDS = 4,    /* a size word or tail-head distance was wrong   */
+  XP_ERR_ABORTED = 5,   /* stopped by xp_abort() or an earlier error     */
+  XP_ERR_INTERNAL = 6
+} xp_status;
+
+/* Protocols ([transfer] copy mode = SIMPLE; [rdma] §4.1 flag-in-data = LL). */
+typedef enum { XP_PROTO_SIMPLE = 0, XP_PROTO_LL = 1 } xp_proto;
+
+/* Where the FIFO (slots and counters) lives: device HBM, or pinned host
+ * memory mapped into the device address space ([setup] shmTransport). */
+typedef enum { XP_PLACE_DEVICE = 0, XP_PLACE_HOST_MAPPED = 1 } xp_placement;
+
+/* Element types of the ring allreduce (add: IEEE fp32 round-to-nearest-even
+ * without FMA or flush-to-zero; int32 wraps modulo 2^32). */
+typedef enum { XP_U8 = 0, XP_U32 = 1, XP_I32 = 2, XP_F32 = 3, XP_BF16 = 4 } xp_dtype;
+
+/* Which device wait reported an error (xp_report.where). */
+typedef enum {
+  XP_WAIT_NONE = 0, XP_WAIT_HEAD = 1, XP_WAIT_TAIL = 2, XP_WAIT_PTR_EXCHANGE = 3,
+  XP_WAIT_LL_FLAG = 4, XP_WAIT_SLOT_BARRIER = 5, XP_WAIT_SIZE_WORD = 6, XP_WAIT_OCCUPANCY = 7,
+  XP_WAIT_STICKY = 8
+} xp_wait_site;
+
+typedef struct xp_fifo xp_fifo;   /* opaque, owned by the library */
+typedef struct xp_ring xp_ring;   /* opaque, owned by the library */
+typedef struct CUstream_st* xp_stream_t;   /* same type as cudaStream_t */
+
+/* Device-side outcome of the last operation on a FIFO or ring. */
+typedef struct {
+  int32_t code;            /* xp_status                                   */
+  int32_t channel;         /* first channel (ring: rank*nchannels+channel) that failed, or -1 */
+  int32_t where;           /* xp_wait_site                                */
+  int32_t reserved;
+  uint64_t observed;       /* counter value seen when the wait gave up    */
+  uint64_t expected;       /* value it waited for                         */
+  uint32_t max_occupancy;  /* largest tail - head a sender published      */
+  uint32_t reserved2;
+} xp_report;
+
+/* Layout of one channel of a FIFO, for tests and tools (xp_fifo_describe).
+ * ctl points at the channel's control block: uint64 tail at +0, uint64 head
+ * at +128, uint64 ptrExchange at +256, uint64 step base at +384 and int64
+ * size words (one per slot, -1 = never written) at +512; slots points at
+ * slot 0, slot k at slots + k * slot_stride.  LL slots hold 16-byte lines
+ * {data0, flag0, data1, flag1} (uint32 each). */
+typedef struct {
+  void* ctl;
+  void* slots;
+  size_t slot_stride;
+  int nslots;
+  int proto;
+  int placement;
+  int lanes;
+} xp_channel_desc;
+
+/* Create a FIFO of `nchannels` independent channels, each with `nslots`
+ * slots of `slot_bytes` bytes ([setup] p2pRecvConnect: N steps of
+ * buffSize / N bytes; [rdma] §7.2: allocated once, reused by every
+ * transfer).  Counters start at 0 and size words at -1.
+ *   1 <= nchannels <= 64, 1 <= nslots <= 64, slot_bytes a non-zero multiple
+ *   of 16 (LL: of 16-byte lines), nchannels * nslots * slot_bytes <= 2^40.
+ * The library owns the memory (cudaMalloc, or cudaHostAlloc(Mapped|Portable)
+ * for XP_PLACE_HOST_MAPPED) and frees it in xp_fifo_destroy.  The FIFO is
+ * bound to the device current at creation.  Errors: XP_ERR_INVALID (bad
+ * argument, *out untouched), XP_ERR_CUDA (allocation failed). */
+xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto proto,
+                         xp_placement place, xp_fifo** out);
+
+/* Synchronise the device, then free the FIFO.  NULL is a no-op. */
+xp_status xp_fifo_destroy(xp_fifo* f);
+
+/* CTAs per channel side: each channel's sender and receiver are each spread
+ * over `lanes` CTAs of one thread-block cluster that share the channel's one
+ * tail and one head (1 <= lanes <= 8; default 1: one sender CTA and one
+ * receiver CTA per channel).  SIMPLE FIFOs only.  Takes effect at the next
+ * operation. */
+xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
+
+/* Channel layout (pointers stay valid until destroy). */
+xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out);
+
+/* Copy `bytes` bytes from src to dst through the FIFO ([transfer] copy mode;
+ * [neuron] §4 POST/POLL).  The buffer is cut into channels of
+ * round_up(ceil(bytes / nchannels), 16) bytes (the last ones shorter or
+ * empty); each channel moves its range in slot-steps of slot_bytes:
+ * sender: wait step < head + nslots, copy into slot step % nslots, write the
+ * slot's size word, publish tail = step + 1 (release); receiver: wait
+ * tail > step (acquire), check the size word, copy out, publish head =
+ * step + 1.  XP_PROTO_SIMPLE: any byte count; XP_PROTO_LL: bytes a multiple
+ * of 8, sent as 16-byte lines {d0, flag, d1, flag} with flag = step + 1 and
+ * no tail ([rdma] §4.1).  src and dst must not overlap.  bytes == 0 is a
+ * no-op returning XP_OK. */
+xp_status xp_send_recv(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream);
+
+/* Zero-copy transfer ([transfer] zero copy, address known only at run time):
+ * per channel the receiver publishes dst + channel offset into the
+ * channel's ptrExchange word once it is empty; the sender reads it and
+ * writes src straight into dst in chunks of at most slot_bytes, publishing
+ * tail per chunk (credit as in xp_send_recv); the receiver returns head per
+ * chunk; the sender empties ptrExchange after the last head.  The FIFO's
+ * slots are not touched.  SIMPLE FIFOs only; any byte count. */
+xp_status xp_send_recv_zero_copy(xp_fifo* f, const void* src, void* dst, size_t bytes,
+                                 xp_stream_t stream);
+
+/* Outcome of the FIFO's last operation.  sync != 0 first waits for the
+ * FIFO's last stream; sync == 0 reads whatever the device has written so far
+ * (XP_OK if the operation is still running without error).  `report` may be
+ * NULL.  Returns the device code (XP_OK, XP_ERR_TIMEOUT, ...). */
+xp_status xp_fifo_status(xp_fifo* f, int sync, xp_report* report);
+
+/* Zero the FIFO's counters, size words, ptrExchange and error state
+ * (synchronous); needed after a device error. */
+xp_status xp_fifo_reset(xp_fifo* f);
+
+/* LL ping-pong for one-way latency: `iters` round trips of one 8-byte line,
+ * A -> B through `ab` and B -> A through `ba` (two LL FIFOs, channel 0 of
+ * each), between two CTAs of one cluster; the device clock (globaltimer)
+ * brackets the loop.  Writes the round-trip total in ns to *elapsed_ns
+ * (synchronous; 1 <= iters <= 1e7). */
+xp_status xp_ll_pingpong(xp_fifo* ab, xp_fifo* ba, int iters, uint64_t* elapsed_ns,
+                         xp_stream_t stream);
+
+/* Create the FIFOs of a virtual ring of `nranks` ranks in this GPU's memory
+ * ([setup] 具体说明: rank r receives from r-1 and sends to r+1): for each
+ * rank and channel one SIMPLE FIFO of nslots x slot_bytes owned by the
+ * receiving rank.  2 <= nranks, nranks * lanes <= 16 (one cluster per
+ * channel), 2 <= nslots <= 64, slot_bytes a non-zero multiple of 16. */
+xp_status xp_ring_create(int nranks, int nchannels, int nslots, size_t slot_bytes, xp_placement place,
+                         xp_ring** out);
+xp_status xp_ring_destroy(xp_ring* r);
+
+/* CTAs per rank per channel (1 <= lanes, nranks * lanes <= 16; default 1). */
+xp_status xp_ring_set_lanes(xp_ring* r, int lanes);
+
+/* Allreduce (sum) of `count` elements of type dt (XP_F32 or XP_I32) over the
+ * ring's ranks: send_bufs[r] / recv_bufs[r] are rank r's input and output
+ * (host arrays of nranks device pointers; in place allowed).  Elements are
+ * cut into channels (16-byte aligned, as xp_send_recv); each channel range is
+ * walked in rounds of nranks chunks of (nslots / 2) * slot_bytes bytes (the
+ * last round shrinks them).  Per round rank r runs send(chunk r-1),
+ * recvReduceSend(chunk r-j) for j = 2..P-1, recvReduceCopySend(chunk r),
+ * recvCopySend(chunk r+1-j) for j = 2..P-1 and recv(chunk r+1), each moved in
+ * slot-steps through its FIFOs, so element i of chunk k ends as
+ * ((x[k+1] + x[k+2]) + ...) + x[k] on every rank. */
+xp_status xp_ring_allreduce_virtual(xp_ring* r, const void* const* send_bufs, void* const* recv_bufs,
+                                    size_t count, xp_dtype dt, xp_stream_t stream);
+
+xp_status xp_ring_status(xp_ring* r, int sync, xp_report* report);
+xp_status xp_ring_reset(xp_ring* r);
+
+/* Spin timeout of every device wait in later launches, in ns (default 2e9;
+ * 1e3 <= ns <= 6e10). */
+xp_status xp_set_spin_timeout_ns(uint64_t ns);
+
+/* Set (value != 0) or clear the process-wide abort word, which lives in
+ * mapped host memory and is polled by every device wait: running and later
+ * operations stop with XP_ERR_ABORTED while it is set. */
+xp_status xp_abort(int value);
+
+const char* xp_status_string(xp_status s);
+/* Message of the last error on the calling thread ("" if none). */
+const char* xp_last_error(void);
+int xp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* XP_H */

@@ -1,0 +1,92 @@
+"""Failure detection without a GPU fault: every device wait is bounded, so a
+wait on a counter that nothing will ever advance ends with a status the host
+reads; the host abort word stops waits early; an object that saw an error
+refuses work until it is reset."""
+import numpy as np
+import pytest
+
+import workloads
+from tests.gpu_util import from_dev, raw_view, to_dev, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = torch_cuda()
+    from collective_transport_plane_gb300 import build
+    build.build()
+    import collective_transport_plane_gb300.xp as xp
+    yield torch, xp
+    xp.xp_abort(0)
+    xp.xp_set_spin_timeout_ns(2_000_000_000)
+
+
+def _stall(torch, xp, fifo):
+    # move the channel's step base far ahead of its head: the sender's first
+    # step needs credit that no receiver will ever return, and the receiver
+    # waits for a tail that no sender will publish
+    d = xp.xp_fifo_describe(fifo, 0)
+    raw_view(torch, d.ctl, 128, "<u8")[48] = 1000
+    torch.cuda.synchronize()
+
+
+def test_wait_times_out_and_reports(env):
+    torch, xp = env
+    xp.xp_set_spin_timeout_ns(50_000_000)
+    fifo = xp.xp_fifo_create(1, 2, 1024)
+    _stall(torch, xp, fifo)
+    src = torch.ones(8192, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros_like(src)
+    xp.xp_send_recv(fifo, src, dst, 8192)
+    st, rep = xp.xp_fifo_status(fifo, True)
+    assert st == xp.XP_ERR_TIMEOUT
+    assert rep.where in (xp.XP_WAIT_HEAD, xp.XP_WAIT_TAIL, xp.XP_WAIT_SLOT_BARRIER)
+    assert rep.channel == 0
+    # sticky: the next operation is refused on the device
+    xp.xp_send_recv(fifo, src, dst, 8192)
+    st, rep = xp.xp_fifo_status(fifo, True)
+    assert st == xp.XP_ERR_ABORTED and rep.where == xp.XP_WAIT_STICKY
+    # reset restores it
+    xp.xp_fifo_reset(fifo)
+    xp.xp_set_spin_timeout_ns(2_000_000_000)
+    xp.xp_send_recv(fifo, src, dst, 8192)
+    st, _ = xp.xp_fifo_status(fifo, True)
+    assert st == xp.XP_OK and bool((dst == 1).all())
+    xp.xp_fifo_destroy(fifo)
+
+
+def test_abort_word_stops_waits(env):
+    torch, xp = env
+    xp.xp_set_spin_timeout_ns(20_000_000_000)
+    fifo = xp.xp_fifo_create(1, 2, 1024)
+    _stall(torch, xp, fifo)
+    xp.xp_abort(1)
+    src = torch.ones(4096, dtype=torch.uint8, device="cuda")
+    dst = torch.zeros_like(src)
+    xp.xp_send_recv(fifo, src, dst, 4096)
+    st, _ = xp.xp_fifo_status(fifo, True)
+    xp.xp_abort(0)
+    xp.xp_set_spin_timeout_ns(2_000_000_000)
+    assert st == xp.XP_ERR_ABORTED
+    xp.xp_fifo_destroy(fifo)
+
+
+def test_ll_flag_wait_times_out(env):
+    # an LL receiver whose flags never arrive: the sender is held back by
+    # a head that never advances
+    torch, xp = env
+    xp.xp_set_spin_timeout_ns(50_000_000)
+    fifo = xp.xp_fifo_create(1, 1, 64, xp.XP_PROTO_LL)
+    _stall(torch, xp, fifo)
+    words = to_dev(torch, workloads.uniform_u32(64, seed=1))
+    out = torch.zeros_like(words)
+    xp.xp_send_recv(fifo, words, out, 256)
+    st, rep = xp.xp_fifo_status(fifo, True)
+    assert st == xp.XP_ERR_TIMEOUT
+    xp.xp_fifo_reset(fifo)
+    xp.xp_set_spin_timeout_ns(2_000_000_000)
+    xp.xp_send_recv(fifo, words, out, 256)
+    st, _ = xp.xp_fifo_status(fifo, True)
+    assert st == xp.XP_OK and np.array_equal(from_dev(out), from_dev(words))
+    xp.xp_fifo_destroy(fifo)

@@ -1,0 +1,179 @@
+"""SIMPLE, zero-copy and host-placed FIFO transfers on the GPU, element by
+element against the CPU oracle on the same seeded inputs."""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests.gpu_util import ctl_words, from_dev, raw_view, to_dev, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@functools.lru_cache(maxsize=2)
+def _multi_input():
+    w = workloads.SIMPLE_MULTI
+    return workloads.normal_bf16_bits(w["nelems"], w["seed"]).view(np.uint8)
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = torch_cuda()
+    from collective_transport_plane_gb300 import build
+    build.build()
+    import collective_transport_plane_gb300.xp as xp
+    xp.xp_set_spin_timeout_ns(2_000_000_000)
+    return torch, xp
+
+
+def _run_simple(torch, xp, src_np, nchan, nslots, slot, lanes=1, place=0, zero_copy=False, fifo=None):
+    own = fifo is None
+    if own:
+        fifo = xp.xp_fifo_create(nchan, nslots, slot, xp.XP_PROTO_SIMPLE, place)
+        xp.xp_fifo_set_lanes(fifo, lanes)
+    src = to_dev(torch, src_np)
+    dst = torch.zeros_like(src)
+    s = torch.cuda.current_stream()
+    if zero_copy:
+        xp.xp_send_recv_zero_copy(fifo, src, dst, src_np.nbytes, s)
+    else:
+        xp.xp_send_recv(fifo, src, dst, src_np.nbytes, s)
+    st, rep = xp.xp_fifo_status(fifo, True)
+    assert st == xp.XP_OK, (st, rep.where, rep.observed, rep.expected)
+    assert rep.max_occupancy <= nslots
+    out = from_dev(dst)
+    if own:
+        xp.xp_fifo_destroy(fifo)
+    return out, rep
+
+
+def test_simple_loopback_workload(env):
+    # 1 MiB of uniform bytes, one sender CTA and one receiver CTA, 8 x 64 KiB
+    torch, xp = env
+    w = workloads.SIMPLE_LOOPBACK
+    src = workloads.uniform_bytes(w["nbytes"], w["seed"])
+    want, fifos, _ = oracle.simple_transfer(src, w["nchannels"], w["nslots"], w["slot_bytes"], seed=0)
+    got, rep = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"])
+    assert np.array_equal(got, want)
+    assert 1 <= rep.max_occupancy <= w["nslots"]
+
+
+@pytest.mark.parametrize("n,nchan,nslots,slot,lanes", [
+    (1, 1, 1, 16, 1), (15, 2, 2, 16, 1), (17, 3, 1, 16, 2), (4095, 3, 2, 64, 1), (65537, 4, 2, 4096, 2),
+    (1000003, 16, 8, 16384, 1), (1000003, 5, 3, 65536, 4), (3 << 20, 2, 8, 65536, 8), (777777, 64, 2, 1024, 1),
+    (12345, 1, 1, 4096, 3)])
+def test_simple_sweep(env, n, nchan, nslots, slot, lanes):
+    torch, xp = env
+    src = workloads.uniform_bytes(n, seed=n % 1000)
+    want, _, _ = oracle.simple_transfer(src, nchan, nslots, slot, seed=1)
+    got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, lanes=lanes)
+    assert np.array_equal(got, want)
+
+
+def test_simple_counters_continue(env):
+    # several operations through one FIFO: device counters end where the
+    # oracle's do, and every result is exact
+    torch, xp = env
+    nchan, nslots, slot = 3, 2, 1024
+    fifo = xp.xp_fifo_create(nchan, nslots, slot)
+    xp.xp_fifo_set_lanes(fifo, 2)
+    fifos = None
+    for i, n in enumerate([5000, 1, 70001, 4096, 3 * 1024 * 7 + 5]):
+        src = workloads.uniform_bytes(n, seed=100 + i)
+        want, fifos, _ = oracle.simple_transfer(src, nchan, nslots, slot, seed=i, fifos=fifos)
+        got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, fifo=fifo)
+        assert np.array_equal(got, want)
+    for c in range(nchan):
+        tail, head, ptrx, base = ctl_words(torch, xp, fifo, c)
+        assert tail == head == base == fifos[c].tail
+        assert ptrx == 0
+    xp.xp_fifo_destroy(fifo)
+
+
+@pytest.mark.parametrize("lanes", [1, 4])
+def test_simple_multichannel_workload(env, lanes):
+    # 1 GiB of bf16 N(0,1), 16 channels of 8 x 512 KiB
+    torch, xp = env
+    w = workloads.SIMPLE_MULTI
+    src = _multi_input()
+    want, _, _ = oracle.simple_transfer(src, w["nchannels"], w["nslots"], w["slot_bytes"], seed=2)
+    got, rep = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"], lanes=lanes)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("n,nchan,nslots,slot,lanes", [
+    (1, 1, 1, 16, 1), (100, 3, 2, 32, 2), (65536 + 7, 4, 2, 4096, 1), (1000003, 16, 8, 16384, 4)])
+def test_zero_copy_sweep(env, n, nchan, nslots, slot, lanes):
+    torch, xp = env
+    src_np = workloads.uniform_bytes(n, seed=7 + n % 100)
+    want, chans, _ = oracle.zero_copy_transfer(src_np, nchan, nslots, slot, seed=3)
+    fifo = xp.xp_fifo_create(nchan, nslots, slot)
+    xp.xp_fifo_set_lanes(fifo, lanes)
+    # poison the staging slots: zero copy must leave them alone
+    views = []
+    for c in range(nchan):
+        d = xp.xp_fifo_describe(fifo, c)
+        v = raw_view(torch, d.slots, nslots * slot, "|u1")
+        v.fill_(0xA5)
+        views.append(v)
+    for rep_i in range(2):
+        got, _ = _run_simple(torch, xp, src_np, nchan, nslots, slot, zero_copy=True, fifo=fifo)
+        assert np.array_equal(got, want)
+    for v in views:
+        assert bool((v == 0xA5).all())
+    for c in range(nchan):
+        tail, head, ptrx, base = ctl_words(torch, xp, fifo, c)
+        assert ptrx == 0 and tail == head == base == 2 * chans[c].tail
+    xp.xp_fifo_destroy(fifo)
+
+
+def test_zero_copy_workload(env):
+    torch, xp = env
+    w = workloads.SIMPLE_MULTI
+    src = _multi_input()
+    want, _, _ = oracle.zero_copy_transfer(src, w["nchannels"], w["nslots"], w["slot_bytes"], seed=2)
+    got, _ = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"], lanes=7, zero_copy=True)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("n,nchan,nslots,slot,lanes", [(4097, 2, 2, 1024, 1), (1 << 20, 8, 8, 65536, 2)])
+def test_host_placed_sweep(env, n, nchan, nslots, slot, lanes):
+    torch, xp = env
+    src = workloads.uniform_bytes(n, seed=11)
+    want, _, _ = oracle.simple_transfer(src, nchan, nslots, slot, seed=4)
+    got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, lanes=lanes, place=xp.XP_PLACE_HOST_MAPPED)
+    assert np.array_equal(got, want)
+
+
+def test_host_placed_workload(env):
+    # 256 MiB fp32 uniform[-1,1), 8 channels of 8 x 1 MiB in pinned host memory
+    torch, xp = env
+    w = workloads.HOST_FIFO
+    src = workloads.uniform_f32(w["nelems"], w["seed"]).view(np.uint8)
+    want, _, _ = oracle.simple_transfer(src, w["nchannels"], w["nslots"], w["slot_bytes"], seed=5)
+    got, _ = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"], lanes=2,
+                         place=xp.XP_PLACE_HOST_MAPPED)
+    assert np.array_equal(got, want)
+
+
+def test_argument_errors(env):
+    torch, xp = env
+    fifo = xp.xp_fifo_create(2, 2, 1024)
+    a = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    b = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    for args in [(a[1:], b, 16), (a, b[3:], 16), (a, a[16:], 64)]:
+        with pytest.raises(xp.XpError) as e:
+            xp.xp_send_recv(fifo, *args)
+        assert e.value.status == xp.XP_ERR_INVALID
+    xp.xp_send_recv(fifo, a, b, 0)            # no-op
+    ll = xp.xp_fifo_create(1, 2, 1024, xp.XP_PROTO_LL)
+    with pytest.raises(xp.XpError):
+        xp.xp_send_recv(ll, a, b, 12)
+    with pytest.raises(xp.XpError):
+        xp.xp_send_recv_zero_copy(ll, a, b, 16)
+    with pytest.raises(xp.XpError):
+        xp.xp_fifo_set_lanes(ll, 2)
+    xp.xp_fifo_destroy(ll)
+    xp.xp_fifo_destroy(fifo)
