@@ -37,7 +37,7 @@ import workloads  # noqa: E402
 METRIC = "FIFO transfer GB/s and % of HBM roofline (SIMPLE, 1 GPU); LL 8 B latency µs"
 GIB = 1 << 30
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["xp_p2p.cu", "xp_device.cuh", "xp_internal.h"]
+KERNEL_SOURCES = ["xp_p2p_tma.cu", "xp_device.cuh", "xp_internal.h"]
 
 
 def dist_env():
@@ -66,7 +66,7 @@ def kernel_source_hash() -> str:
 def profiled_traffic():
     """DRAM bytes per launch of the timed kernel from the committed ncu summary,
     if the kernel sources have not changed since it was captured."""
-    path = os.path.join(ROOT, "profiles", "p2p_simple_1GiB_16ch.md")
+    path = os.path.join(ROOT, "profiles", "p2p_tma_simple_1GiB_16ch.md")
     try:
         txt = open(path).read()
     except OSError:
@@ -199,9 +199,11 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--lanes", type=int, default=4)
+    ap.add_argument("--lanes", type=int, default=6)
     ap.add_argument("--no-rows", action="store_true", help="time the step only")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--mib", type=int, default=0,
+                    help="profiling only: move the first MiB of the workload instead of 1 GiB")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -222,7 +224,7 @@ def main():
 
     hbm_peak, peak_kind = peaks()
     w = workloads.SIMPLE_MULTI
-    src_np = workloads.normal_bf16_bits(w["nelems"], w["seed"])
+    src_np = workloads.normal_bf16_bits((args.mib << 19) if args.mib else w["nelems"], w["seed"])
     nbytes = src_np.nbytes
     src = torch.from_numpy(src_np).to("cuda")
     dst = torch.empty_like(src)
@@ -281,6 +283,8 @@ def main():
         "clocks": clk,
     }
 
+    if args.mib:
+        out["config"]["workload"] += f" (profiling case: first {args.mib} MiB)"
     if rank == 0 and not args.no_rows:
         out["e2e"] = e2e_row(torch, xp, fifo, src_np, stream)
         out["rows"] = rows(torch, xp, hbm_peak)
@@ -338,7 +342,7 @@ def rows(torch, xp, hbm_peak):
     dst = torch.empty_like(src)
     n = src.numel() * 2
     zc = {}
-    for lanes in (4, 7):
+    for lanes in (4, 8):
         f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
         xp.xp_fifo_set_lanes(f, lanes)
         with torch.cuda.stream(s):

@@ -17,6 +17,9 @@
 
 namespace xp {
 void* p2p_kernel_ptr(bool zero_copy);
+void* p2p_tma_kernel_ptr(bool zero_copy);
+int p2p_tma_threads();
+int p2p_tma_smem();
 void* ll_kernel_ptr();
 void* ll_pingpong_kernel_ptr();
 void* ring_kernel_ptr(int dtype);
@@ -174,11 +177,12 @@ xp_status read_status(Common& c, int sync, xp_report* rep) {
 // Cluster co-residency: every cluster of the launch must fit on the GPU.
 std::map<std::tuple<const void*, int, int>, int> g_fits;
 
-xp_status launch(const void* kernel, int grid, int block, int csize, void* params, cudaStream_t stream) {
+xp_status launch(const void* kernel, int grid, int block, int csize, void* params, cudaStream_t stream,
+                 int smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(block, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -193,6 +197,7 @@ xp_status launch(const void* kernel, int grid, int block, int csize, void* param
     auto it = g_fits.find(key);
     if (it == g_fits.end()) {
       if (csize > 8) XP_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+      if (smem > 48 * 1024) XP_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
       int n = 0;
       XP_CUDA(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
       it = g_fits.emplace(key, n).first;
@@ -357,21 +362,29 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   p.abort_word = g_abort_dev;
   p.timeout_ns = g_timeout_ns.load();
   const void* kernel;
-  int csize, block;
+  int csize, block, smem = 0;
   if (f->proto == XP_PROTO_LL) {
     kernel = xp::ll_kernel_ptr();
     p.lanes = 1;
     csize = 2;
     block = xp::kLLThreads;
   } else {
-    kernel = xp::p2p_kernel_ptr(zero_copy);
     p.lanes = f->lanes;
     csize = zero_copy ? f->lanes + 1 : 2 * f->lanes;
-    block = xp::kP2pThreads;
+    if (f->place == XP_PLACE_DEVICE) {
+      // HBM FIFO: bulk copies through shared memory
+      kernel = xp::p2p_tma_kernel_ptr(zero_copy);
+      block = xp::p2p_tma_threads();
+      smem = xp::p2p_tma_smem();
+    } else {
+      // mapped host FIFO: 16-byte vector loads and stores from every warp
+      kernel = xp::p2p_kernel_ptr(zero_copy);
+      block = xp::kP2pThreads;
+    }
   }
   p.csize = csize;
   XP_CUDA(cudaMemsetAsync(f->cm.status, 0, xp::kStatusClearBytes, st));
-  if ((s = launch(kernel, f->C * csize, block, csize, &p, st)) != XP_OK) return s;
+  if ((s = launch(kernel, f->C * csize, block, csize, &p, st, smem)) != XP_OK) return s;
   XP_CUDA(cudaEventRecord(f->cm.done, st));
   f->cm.used = true;
   return XP_OK;

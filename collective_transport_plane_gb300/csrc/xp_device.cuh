@@ -101,8 +101,11 @@ __device__ __forceinline__ void report(const WaitCtx& w, int code, int where, u6
   atomicExch(&w.st->abort, 1);
 }
 
+__device__ __forceinline__ bool op_aborted_device(const WaitCtx& w) {
+  return *reinterpret_cast<volatile int*>(&w.st->abort) != 0;
+}
 __device__ __forceinline__ bool op_aborted(const WaitCtx& w) {
-  if (*reinterpret_cast<volatile int*>(&w.st->abort)) return true;
+  if (op_aborted_device(w)) return true;
   if (w.abort_word && *w.abort_word) {
     report(w, XP_ERR_ABORTED, XP_WAIT_NONE, 0, 0);
     return true;
@@ -110,11 +113,48 @@ __device__ __forceinline__ bool op_aborted(const WaitCtx& w) {
   return false;
 }
 
+// Clock of one bounded wait.  The first kQuietNs of a wait only spin; after
+// that the operation's abort flag (device memory) is checked every
+// kCheckNs, the host abort word (mapped host memory, a slow read) every
+// kHostCheckNs, and the wait gives up after timeout_ns.
+constexpr u64 kQuietNs = 20000;
+constexpr u64 kCheckNs = 20000;
+constexpr u64 kHostCheckNs = 200000;
+
+struct WaitClock {
+  u64 start = 0, next = 0, next_host = 0;
+  // false: stop waiting (the reason is already reported)
+  __device__ __forceinline__ bool tick(const WaitCtx& w, int where, u64 observed, u64 expected) {
+    const u64 now = globaltimer();
+    if (start == 0) {
+      start = now;
+      next = now + kQuietNs;
+      next_host = now + kHostCheckNs;
+      return true;
+    }
+    if (now < next) return true;
+    next = now + kCheckNs;
+    if (op_aborted_device(w)) return false;
+    if (now >= next_host) {
+      next_host = now + kHostCheckNs;
+      if (w.abort_word && *w.abort_word) {
+        report(w, XP_ERR_ABORTED, XP_WAIT_NONE, 0, 0);
+        return false;
+      }
+    }
+    if (now - start > w.timeout_ns) {
+      report(w, XP_ERR_TIMEOUT, where, observed, expected);
+      return false;
+    }
+    return true;
+  }
+};
+
 // Poll `*p` (acquire) until it is >= target.  One thread.  Gives up on the
 // operation's abort flag, the host abort word, or after timeout_ns.
 static __device__ __noinline__ bool wait_geq(const u64* p, u64 target, u64& cache, const WaitCtx& w, int where) {
   if (cache >= target) return true;
-  u64 start = 0;
+  WaitClock clk;
   unsigned it = 0;
   for (;;) {
     u64 v = ld_acquire(p);
@@ -122,22 +162,13 @@ static __device__ __noinline__ bool wait_geq(const u64* p, u64 target, u64& cach
       cache = v;
       return true;
     }
-    if ((++it & 127u) == 0) {
-      if (op_aborted(w)) return false;
-      u64 now = globaltimer();
-      if (start == 0) {
-        start = now;
-      } else if (now - start > w.timeout_ns) {
-        report(w, XP_ERR_TIMEOUT, where, v, target);
-        return false;
-      }
-    }
+    if ((++it & 7u) == 0 && !clk.tick(w, where, v, target)) return false;
   }
 }
 
 // Same for a word that must become zero (mode 0) or non-zero (mode 1).
 static __device__ __noinline__ bool wait_word(const u64* p, int nonzero, u64& value, const WaitCtx& w, int where) {
-  u64 start = 0;
+  WaitClock clk;
   unsigned it = 0;
   for (;;) {
     u64 v = ld_acquire(p);
@@ -145,16 +176,7 @@ static __device__ __noinline__ bool wait_word(const u64* p, int nonzero, u64& va
       value = v;
       return true;
     }
-    if ((++it & 127u) == 0) {
-      if (op_aborted(w)) return false;
-      u64 now = globaltimer();
-      if (start == 0) {
-        start = now;
-      } else if (now - start > w.timeout_ns) {
-        report(w, XP_ERR_TIMEOUT, where, v, nonzero ? 1 : 0);
-        return false;
-      }
-    }
+    if ((++it & 7u) == 0 && !clk.tick(w, where, v, nonzero ? 1 : 0)) return false;
   }
 }
 
@@ -173,19 +195,9 @@ __device__ __forceinline__ bool warp_wait_geq(const u64* p, u64 target, u64& cac
 }
 
 static __device__ __noinline__ bool mbar_wait(uint32_t saddr, uint32_t parity, const WaitCtx& w, int where, u64 step) {
-  u64 start = 0;
-  unsigned it = 0;
+  WaitClock clk;
   while (!mbar_try_wait(saddr, parity)) {
-    if ((++it & 15u) == 0) {
-      if (op_aborted(w)) return false;
-      u64 now = globaltimer();
-      if (start == 0) {
-        start = now;
-      } else if (now - start > w.timeout_ns) {
-        report(w, XP_ERR_TIMEOUT, where, step, step + 1);
-        return false;
-      }
-    }
+    if (!clk.tick(w, where, step, step + 1)) return false;
   }
   return true;
 }
@@ -248,6 +260,107 @@ __device__ __forceinline__ void channel_range(u64 n, int C, int c, u64* lo, u64*
   u64 a = q * c, b = q * (c + 1);
   *lo = a < n ? a : n;
   *hi = b < n ? b : n;
+}
+
+}  // namespace xp
+
+namespace xp {
+
+// ---- bulk (TMA) copies between global and shared memory, 16-byte granular
+__device__ __forceinline__ void mbar_arrive_local(uint32_t saddr) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr) : "memory");
+}
+// Arm a stage barrier for `bytes` of bulk-copy data.  Relaxed: the thread
+// that arms it is the one that waits on it, so it orders nothing else.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t saddr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cta.shared::cta.b64 _, [%0], %1;" ::"r"(saddr), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_local_relaxed(uint32_t saddr) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(saddr) : "memory");
+}
+// Relaxed arrive on an mbarrier anywhere in the cluster: for signals that
+// carry no memory ordering (the reads they report have already completed).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_saddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_saddr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cta(uint32_t saddr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a CTA-local mbarrier phase.
+static __device__ __noinline__ bool mbar_wait_cta(uint32_t saddr, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait_cta(saddr, parity)) return true;
+  WaitClock clk;
+  while (!mbar_try_wait_cta(saddr, parity)) {
+    if (!clk.tick(w, XP_WAIT_SLOT_BARRIER, parity, 0)) return false;
+  }
+  return true;
+}
+// L2 cache policies for bulk copies: FIFO slots are recycled every N steps and
+// should stay in L2 (evict_last); user buffers stream through once (evict_first).
+__device__ __forceinline__ u64 policy_evict_last() {
+  u64 p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ u64 policy_evict_first() {
+  u64 p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar, u64 policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(sdst), "l"(gsrc), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes, u64 policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+               "r"(ssrc), "r"(bytes), "l"(policy) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// A counter mirrored in shared memory by a watcher thread of the same CTA.
+__device__ __forceinline__ u64 ld_acquire_cta_shared(const u64* p) {
+  u64 v;
+  asm volatile("ld.acquire.cta.shared::cta.u64 %0, [%1];" : "=l"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_cta_shared(u64* p, u64 v) {
+  asm volatile("st.release.cta.shared::cta.u64 [%0], %1;" ::"r"(smem_addr(p)), "l"(v) : "memory");
+}
+// Wait until the mirrored counter is >= target (one thread).
+static __device__ __noinline__ bool wait_mirror(const u64* m, u64 target, u64& cache, const WaitCtx& w, int where) {
+  if (cache >= target) return true;
+  WaitClock clk;
+  for (;;) {
+    const u64 v = ld_acquire_cta_shared(m);
+    if (v >= target) {
+      cache = v;
+      return true;
+    }
+    if (!clk.tick(w, where, v, target)) return false;
+  }
+}
+
+// Order this thread's async-proxy (bulk copy) accesses of global memory with
+// its generic-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 }  // namespace xp

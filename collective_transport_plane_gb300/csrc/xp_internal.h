@@ -4,7 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/xp.h"
+#include "xp.h"
 
 namespace xp {
 

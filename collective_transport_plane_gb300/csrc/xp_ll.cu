@@ -91,21 +91,14 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
         const char* slot = slots + (step % N) * p.slot_bytes;
         for (u64 i = tid; i < nl && !failed; i += T) {
           u64 a, b;
-          u64 start = 0;
+          WaitClock clk;
           unsigned it = 0;
           for (;;) {
             ll_load(slot + 16 * i, a, b);
             if ((uint32_t)(a >> 32) == flag && (uint32_t)(b >> 32) == flag) break;
-            if ((++it & 255u) == 0) {
-              if (op_aborted(w)) { failed = 1; break; }
-              const u64 now = globaltimer();
-              if (start == 0) {
-                start = now;
-              } else if (now - start > w.timeout_ns) {
-                report(w, XP_ERR_TIMEOUT, XP_WAIT_LL_FLAG, (a >> 32) | ((b >> 32) << 32), flag);
-                failed = 1;
-                break;
-              }
+            if ((++it & 7u) == 0 && !clk.tick(w, XP_WAIT_LL_FLAG, (a >> 32) | ((b >> 32) << 32), flag)) {
+              failed = 1;
+              break;
             }
           }
           if (!failed) __stcs(dst + first + i, make_uint2((uint32_t)a, (uint32_t)b));
@@ -161,21 +154,13 @@ __global__ void __launch_bounds__(32, 1) ll_pingpong_kernel(const PingParams p) 
       const u64 r = rbase + i;
       const uint32_t f = (uint32_t)(r + 1);
       const char* line = rslots + (r % Nr) * Sr;
-      u64 a, b, start = 0;
+      u64 a, b;
+      WaitClock clk;
       unsigned it = 0;
       for (;;) {
         ll_load(line, a, b);
         if ((uint32_t)(a >> 32) == f && (uint32_t)(b >> 32) == f) break;
-        if ((++it & 255u) == 0) {
-          if (op_aborted(w)) return false;
-          const u64 now = globaltimer();
-          if (start == 0) {
-            start = now;
-          } else if (now - start > w.timeout_ns) {
-            report(w, XP_ERR_TIMEOUT, XP_WAIT_LL_FLAG, a >> 32, f);
-            return false;
-          }
-        }
+        if ((++it & 7u) == 0 && !clk.tick(w, XP_WAIT_LL_FLAG, a >> 32, f)) return false;
       }
       if ((uint32_t)a != (uint32_t)i || (uint32_t)b != ((uint32_t)i ^ 0x5a5a5a5au)) {
         report(w, XP_ERR_BOUNDS, XP_WAIT_LL_FLAG, a, i);

@@ -1,0 +1,407 @@
+// SIMPLE and zero-copy channel kernels for FIFOs in HBM, data moved with bulk
+// (TMA) copies through shared memory.
+//
+// Cluster layout as in the vector kernels (xp_p2p.cu): per channel, CTAs
+// [0, G) send and [G, 2G) receive (zero copy: CTA G receives).  Each CTA moves
+// one contiguous stripe of every slot-step ("lane") through a ring of
+// kTmaStages shared-memory stages:
+//   sender    - one mover thread issues bulk loads from src up to kLookSend
+//               entries ahead (they need nothing) and bulk stores into the
+//               slot (they need credit);
+//   receiver  - a loader thread waits for tail and bulk-loads the slot into
+//               free stages, a storer thread bulk-stores each stage into dst
+//               and frees it, so neither stream waits for the other's
+//               memory latency;
+//   watcher   - polls the one remote counter the CTA waits on (sender: head,
+//               receiver: tail) and mirrors it into shared memory, so no
+//               copying thread stalls on a global-memory round trip;
+//   publisher - in the side's leader CTA only: waits until all G lanes have
+//               signalled a slot-step on its mbarrier and publishes the one
+//               channel-wide counter (tail = step + 1 on the sender side,
+//               head = step + 1 on the receiver side).
+// A sender stripe is signalled once its bulk stores have completed.  The mover
+// checks that only after kDefer stores of the next step are in flight, so the
+// store pipeline never drains at a step boundary, and before it blocks on
+// credit it reports whatever is pending (a FIFO of one slot would otherwise
+// wait on itself).  It reports through shared memory to a signaler thread,
+// which does the cluster-scope release arrive: a release waits for the
+// issuing thread's in-flight memory traffic, and the mover always has some.  A receiver stripe is signalled as soon as its
+// bulk loads from the slot have landed in shared memory.  Slot traffic is
+// marked evict_last in L2 and user-buffer traffic evict_first, so the FIFO
+// stays L2-resident while src and dst stream through.
+#include <cuda_runtime.h>
+
+#include "xp_device.cuh"
+
+namespace xp {
+
+constexpr int kTmaStages = 6;
+constexpr uint32_t kTmaChunk = 16384;
+// Loads issued ahead of the next store; the other stages hold stores that
+// are still reading shared memory.  The slow side of each role gets the depth:
+// the SIMPLE sender loads from HBM and stores into the (L2-resident) slot, the
+// receiver loads from the slot and stores into HBM, zero copy goes HBM to HBM.
+constexpr int kLookSend = 4;
+constexpr int kLookZeroCopy = 3;
+constexpr int kRecvStoresInFlight = 3;   // receiver: dst stores still reading their stage
+constexpr int kTmaThreads = 128;
+constexpr int kTmaSmem = kTmaStages * (int)kTmaChunk;
+constexpr int kDefer = 4;
+static_assert(kLookSend < kTmaStages && kLookZeroCopy < kTmaStages && kRecvStoresInFlight < kTmaStages,
+              "a stage must be free for each look-ahead load");
+
+// The stripe of one slot-step a lane moves: [b0, b0 + fb) in bulk entries of
+// at most kTmaChunk bytes (at least one entry, possibly empty), then `rag`
+// (< 16) bytes moved by the thread itself.
+struct Stripe {
+  u64 b0, fb, rag, nent;
+};
+
+__device__ __forceinline__ Stripe stripe_of(u64 sz, u64 lanes, u64 lane) {
+  u64 b0, b1;
+  piece(sz, lanes, lane, &b0, &b1);
+  Stripe s;
+  s.b0 = b0;
+  const u64 n = b1 - b0;
+  s.fb = n & ~15ull;
+  s.rag = n - s.fb;
+  s.nent = s.fb ? (s.fb + kTmaChunk - 1) / kTmaChunk : 1;
+  return s;
+}
+
+__device__ __forceinline__ uint32_t entry_bytes(const Stripe& s, u64 e) {
+  const u64 eo = e * kTmaChunk;
+  if (eo >= s.fb) return 0;
+  const u64 n = s.fb - eo;
+  return (uint32_t)(n < kTmaChunk ? n : kTmaChunk);
+}
+
+__device__ __forceinline__ void copy_bytes(const char* src, char* dst, u64 n) {
+  for (u64 i = 0; i < n; ++i) dst[i] = __ldcg(src + i);
+}
+
+// Entry numbering of one lane over all slot-steps of an operation: every
+// step but the last has the stripe of a full slot, the last its own.
+struct Entries {
+  Stripe full, last;
+  u64 nsteps, per_full, total;
+  __device__ __forceinline__ void init(u64 len, u64 S, u64 G, u64 lane) {
+    nsteps = (len + S - 1) / S;
+    const u64 last_sz = len - (nsteps - 1) * S;
+    full = stripe_of(nsteps > 1 ? S : last_sz, G, lane);
+    last = stripe_of(last_sz, G, lane);
+    per_full = nsteps > 1 ? full.nent : 0;
+    total = per_full * (nsteps - 1) + last.nent;
+  }
+  // step and entry-within-step of global entry j
+  __device__ __forceinline__ void locate(u64 j, u64* s, u64* e) const {
+    const u64 nf = per_full * (nsteps - 1);
+    if (j < nf) {
+      *s = j / per_full;
+      *e = j - *s * per_full;
+    } else {
+      *s = nsteps - 1;
+      *e = j - nf;
+    }
+  }
+  __device__ __forceinline__ const Stripe& stripe(u64 s) const { return s + 1 == nsteps ? last : full; }
+};
+
+template <bool kZeroCopy>
+__global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams p) {
+  extern __shared__ __align__(128) char stage_mem[];
+  __shared__ __align__(8) u64 bars[kMaxSlots];
+  __shared__ __align__(8) u64 full[kTmaStages];
+  __shared__ __align__(8) u64 empty[kTmaStages];   // receiver: stage free again
+  __shared__ u64 s_base;
+  __shared__ u64 s_mirror;   // latest head (sender) or tail (receiver) seen by the watcher
+  __shared__ u64 s_done;     // sender: steps [0, s_done) have their bulk stores complete
+  __shared__ int s_stop;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const unsigned crank = cluster_ctarank();
+  const int ch = blockIdx.x / p.csize;
+  const int G = p.lanes;
+  const bool sender = crank < (unsigned)G;
+  const int lane_id = sender ? (int)crank : (int)crank - G;
+  const unsigned leader = sender ? 0u : (unsigned)G;
+  const bool leader_cta = crank == leader;
+  const u64 N = (u64)p.nslots;
+  const u64 S = p.slot_bytes;
+  const u64 K = kTmaStages;
+
+  char* ctl = p.ctl + (u64)ch * kCtlBytes;
+  u64* tail = reinterpret_cast<u64*>(ctl + kTailOff);
+  u64* head = reinterpret_cast<u64*>(ctl + kHeadOff);
+  u64* ptrx = reinterpret_cast<u64*>(ctl + kPtrxOff);
+  u64* basew = reinterpret_cast<u64*>(ctl + kBaseOff);
+  long long* sizew = reinterpret_cast<long long*>(ctl + kSizeOff);
+  char* slots = p.slots + (u64)ch * p.ch_stride;
+
+  u64 lo, hi;
+  channel_range(p.nbytes, p.nchannels, ch, &lo, &hi);
+  const u64 len = hi - lo;
+  const u64 nsteps = (len + S - 1) / S;
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch};
+
+  if (threadIdx.x == 0) {
+    s_base = ld_relaxed(basew);
+    s_stop = 0;
+    if (*reinterpret_cast<volatile int*>(&p.status->sticky)) {
+      s_stop = 1;
+      if (atomicCAS(&p.status->code, 0, XP_ERR_ABORTED) == 0) {
+        p.status->channel = ch;
+        p.status->where = XP_WAIT_STICKY;
+      }
+    }
+    s_mirror = 0;
+    s_done = 0;
+    for (int k = 0; k < kTmaStages; ++k) {
+      mbar_init(smem_addr(&full[k]), 1);
+      mbar_init(smem_addr(&empty[k]), 1);
+    }
+    if (leader_cta)
+      for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), (uint32_t)G);
+    mbar_init_fence();
+  }
+  cluster_sync_all();
+  const u64 base = s_base;
+  const bool run = nsteps > 0 && s_stop == 0;
+  const uint32_t sm0 = smem_addr(stage_mem);
+  const uint32_t bar0 = map_to_rank(smem_addr(&bars[0]), leader);
+  const u64 pol_slot = policy_evict_last();     // FIFO slots: reused every N steps
+  const u64 pol_user = policy_evict_first();    // src / dst: read or written once
+
+  if (run && lane == 0) {
+    if (kZeroCopy && !sender) {
+      if (warp == 1) {
+        // zero-copy receiver: post the destination, echo tail into head
+        u64 v = 0, tcache = 0;
+        if (wait_word(ptrx, 0, v, w, XP_WAIT_PTR_EXCHANGE)) {
+          st_release(ptrx, reinterpret_cast<u64>(p.dst + lo));
+          u64 j = 0;
+          for (; j < nsteps; ++j) {
+            if (!wait_geq(tail, base + j + 1, tcache, w, XP_WAIT_TAIL)) break;
+            st_release(head, base + j + 1);
+          }
+          if (j == nsteps) st_relaxed(basew, base + nsteps);
+        }
+      }
+    } else if (warp == 0) {
+      Entries en;
+      en.init(len, S, (u64)G, (u64)lane_id);
+      const u64 total = en.total;
+      u64 jl = 0;   // next entry to load
+      u64 j = 0;    // next entry to store
+      bool ok = true;
+      if (sender) {
+        // ---------------- sender mover ----------------
+        constexpr int kLook = kZeroCopy ? kLookZeroCopy : kLookSend;
+        auto issue_load = [&](u64 q) {
+          u64 s, e;
+          en.locate(q, &s, &e);
+          const Stripe& st = en.stripe(s);
+          const uint32_t k = (uint32_t)(q % K);
+          const uint32_t nb = entry_bytes(st, e);
+          mbar_arrive_expect_tx(smem_addr(&full[k]), nb);
+          if (nb)
+            bulk_load(sm0 + k * kTmaChunk, p.src + lo + s * S + st.b0 + e * kTmaChunk, nb, smem_addr(&full[k]), pol_user);
+        };
+        for (; jl < total && jl < (u64)kLook; ++jl) issue_load(jl);
+        char* dstp = nullptr;
+        if (kZeroCopy) {
+          u64 v = 0;
+          ok = wait_word(ptrx, 1, v, w, XP_WAIT_PTR_EXCHANGE);
+          dstp = reinterpret_cast<char*>(v);
+        }
+        u64 hcache = 0;
+        long long pending = -1;   // step whose completion signal is deferred
+        int since = 0;
+        for (u64 s = 0; s < nsteps && ok; ++s) {
+          const u64 step = base + s;
+          if (step + 1 > N && hcache < step + 1 - N) {
+            const u64 h = ld_acquire_cta_shared(&s_mirror);
+            if (h >= step + 1 - N) {
+              hcache = h;
+            } else {
+              if (pending >= 0) {
+                bulk_wait<0>();
+                fence_proxy_async_global();
+                st_release_cta_shared(&s_done, (u64)pending + 1);
+                pending = -1;
+              }
+              if (!wait_mirror(&s_mirror, step + 1 - N, hcache, w, XP_WAIT_HEAD)) { ok = false; break; }
+            }
+          }
+          fence_proxy_async_global();
+          const u64 off = s * S;
+          const Stripe& st = en.stripe(s);
+          char* to = kZeroCopy ? dstp + off : slots + (step % N) * S;
+          for (u64 e = 0; e < st.nent; ++e, ++j) {
+            const uint32_t k = (uint32_t)(j % K);
+            if (!mbar_wait_cta(smem_addr(&full[k]), (uint32_t)((j / K) & 1), w)) { ok = false; break; }
+            const uint32_t nb = entry_bytes(st, e);
+            if (nb) bulk_store(to + st.b0 + e * kTmaChunk, sm0 + k * kTmaChunk, nb, kZeroCopy ? pol_user : pol_slot);
+            bulk_commit();
+            if (jl < total) {
+              // the stage of entry jl last held entry jl - K, whose store is
+              // at least K - kLook groups old
+              bulk_wait_read<kTmaStages - kLook - 1>();
+              issue_load(jl++);
+            }
+            if (pending >= 0 && ++since == kDefer) {
+              bulk_wait<kDefer>();
+              fence_proxy_async_global();
+              st_release_cta_shared(&s_done, (u64)pending + 1);
+              pending = -1;
+            }
+          }
+          if (!ok) break;
+          if (st.rag) copy_bytes(p.src + lo + off + st.b0 + st.fb, to + st.b0 + st.fb, st.rag);
+          if (!kZeroCopy && lane_id == 0) sizew[step % N] = (long long)((len - off) < S ? (len - off) : S);
+          if (pending >= 0) {
+            bulk_wait<0>();
+            fence_proxy_async_global();
+            st_release_cta_shared(&s_done, (u64)pending + 1);
+          }
+          pending = (long long)s;
+          since = 0;
+        }
+        bulk_wait<0>();
+        if (ok && pending >= 0) {
+          fence_proxy_async_global();
+          st_release_cta_shared(&s_done, (u64)pending + 1);
+        }
+      } else {
+        // ---------------- receiver loader ----------------
+        // waits for tail (mirrored), copies the step's ragged bytes, and
+        // loads the stripe's entries from the slot as stages become free
+        u64 tcache = 0;
+        for (u64 s = 0; s < nsteps && ok; ++s) {
+          const u64 step = base + s;
+          if (!wait_mirror(&s_mirror, step + 1, tcache, w, XP_WAIT_TAIL)) { ok = false; break; }
+          fence_proxy_async_global();
+          const u64 off = s * S;
+          const u64 sz = (len - off) < S ? (len - off) : S;
+          const char* from = slots + (step % N) * S;
+          if (lane_id == 0) {
+            const long long got = (long long)ld_relaxed(reinterpret_cast<const u64*>(sizew + step % N));
+            if (got != (long long)sz) report(w, XP_ERR_BOUNDS, XP_WAIT_SIZE_WORD, (u64)got, sz);
+          }
+          const Stripe& st = en.stripe(s);
+          if (st.rag) copy_bytes(from + st.b0 + st.fb, p.dst + lo + off + st.b0 + st.fb, st.rag);
+          for (u64 e = 0; e < st.nent; ++e, ++jl) {
+            const uint32_t k = (uint32_t)(jl % K);
+            if (jl >= K && !mbar_wait_cta(smem_addr(&empty[k]), (uint32_t)(((jl / K) - 1) & 1), w)) {
+              ok = false;
+              break;
+            }
+            const uint32_t nb = entry_bytes(st, e);
+            mbar_arrive_expect_tx(smem_addr(&full[k]), nb);
+            if (nb) bulk_load(sm0 + k * kTmaChunk, from + st.b0 + e * kTmaChunk, nb, smem_addr(&full[k]), pol_slot);
+          }
+        }
+      }
+      // every issued load must land before the CTA may exit
+      for (u64 i = (jl > K ? jl - K : 0); i < jl; ++i)
+        mbar_wait_cta(smem_addr(&full[i % K]), (uint32_t)((i / K) & 1), w);
+    } else if (warp == 1 && sender) {
+      // ---------------- sender signaler ----------------
+      // Turns each "stores of step s complete" from the mover into the
+      // cluster-scope release arrive on the slot's barrier in the leader
+      // CTA.  A release waits for the issuing thread's own memory traffic;
+      // this thread has none in flight, the mover always has.
+      u64 done = 0;
+      for (u64 s = 0; s < nsteps; ++s) {
+        if (!wait_mirror(&s_done, s + 1, done, w, XP_WAIT_SLOT_BARRIER)) break;
+        mbar_arrive_cluster(bar0 + 8u * (uint32_t)((base + s) % N));
+      }
+    } else if (warp == 1 && !sender) {
+      // ---------------- receiver storer ----------------
+      // stores each loaded entry into dst; once the last entry of a step is
+      // in shared memory the stripe of the slot has been read: signal it
+      Entries en;
+      en.init(len, S, (u64)G, (u64)lane_id);
+      u64 j = 0;
+      bool ok = true;
+      for (u64 s = 0; s < nsteps && ok; ++s) {
+        const Stripe& st = en.stripe(s);
+        for (u64 e = 0; e < st.nent; ++e, ++j) {
+          const uint32_t k = (uint32_t)(j % K);
+          if (!mbar_wait_cta(smem_addr(&full[k]), (uint32_t)((j / K) & 1), w)) { ok = false; break; }
+          // The slot's bytes for this stripe are in shared memory (its ragged
+          // bytes were copied before the first load of the step): the reads
+          // are complete, so the signal carries no ordering.
+          if (e + 1 == st.nent) mbar_arrive_cluster_relaxed(bar0 + 8u * (uint32_t)((base + s) % N));
+          const uint32_t nb = entry_bytes(st, e);
+          if (nb) bulk_store(p.dst + lo + s * S + st.b0 + e * kTmaChunk, sm0 + k * kTmaChunk, nb, pol_user);
+          bulk_commit();
+          bulk_wait_read<kRecvStoresInFlight>();
+          if (j >= (u64)kRecvStoresInFlight) mbar_arrive_local_relaxed(smem_addr(&empty[(j - kRecvStoresInFlight) % K]));
+        }
+      }
+      bulk_wait<0>();
+    } else if (warp == 2) {
+      // ---------------- watcher ----------------
+      // sender: head, as far as the last step's credit needs it;
+      // receiver: tail, up to the last step
+      const u64* word = sender ? head : tail;
+      const u64 target = sender ? (base + nsteps > N ? base + nsteps - N : 0) : base + nsteps;
+      u64 seen = 0;
+      WaitClock clk;
+      while (seen < target) {
+        const u64 v = ld_acquire(word);
+        if (v > seen) {
+          seen = v;
+          st_release_cta_shared(&s_mirror, v);
+          clk = WaitClock();   // the timeout counts time without progress
+        } else if (!clk.tick(w, sender ? XP_WAIT_HEAD : XP_WAIT_TAIL, v, target)) {
+          break;
+        }
+      }
+    } else if (warp == 3 && leader_cta) {
+      // ---------------- publisher ----------------
+      u64 s = 0;
+      unsigned max_occ = 0;
+      for (; s < nsteps; ++s) {
+        const u64 step = base + s;
+        if (!mbar_wait(smem_addr(&bars[step % N]), (uint32_t)((s / N) & 1), w, XP_WAIT_SLOT_BARRIER, step)) break;
+        if (sender) {
+          st_release(tail, step + 1);
+          const u64 h = ld_relaxed(head);
+          const u64 occ = step + 1 - h;
+          if (h > step + 1 || occ > N) {
+            report(w, XP_ERR_BOUNDS, XP_WAIT_OCCUPANCY, occ, N);
+            break;
+          }
+          if (occ > max_occ) max_occ = (unsigned)occ;
+        } else {
+          st_release(head, step + 1);
+        }
+      }
+      if (sender) {
+        atomicMax(&p.status->max_occupancy, max_occ);
+        if (kZeroCopy && s == nsteps) {
+          u64 hc = 0;
+          if (wait_geq(head, base + nsteps, hc, w, XP_WAIT_HEAD)) st_release(ptrx, 0);
+        }
+      } else if (s == nsteps) {
+        st_relaxed(basew, base + nsteps);
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync_all();
+}
+
+template __global__ void p2p_tma_kernel<false>(const P2pParams);
+template __global__ void p2p_tma_kernel<true>(const P2pParams);
+
+void* p2p_tma_kernel_ptr(bool zero_copy) {
+  return zero_copy ? reinterpret_cast<void*>(&p2p_tma_kernel<true>) : reinterpret_cast<void*>(&p2p_tma_kernel<false>);
+}
+int p2p_tma_threads() { return kTmaThreads; }
+int p2p_tma_smem() { return kTmaSmem; }
+
+}  // namespace xp
