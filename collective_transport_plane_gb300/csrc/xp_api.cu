@@ -214,6 +214,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+namespace xp {
+// Sets the message xp_last_error() returns on this thread.
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace xp
+
 struct xp_fifo {
   Common cm;
   int C = 0, N = 0;

@@ -27,6 +27,7 @@ EXPORTS = [
     "xp_send_recv_zero_copy", "xp_fifo_status", "xp_fifo_reset", "xp_ll_pingpong", "xp_ring_create",
     "xp_ring_destroy", "xp_ring_set_lanes", "xp_ring_allreduce_virtual", "xp_ring_status", "xp_ring_reset",
     "xp_set_spin_timeout_ns", "xp_abort", "xp_status_string", "xp_last_error", "xp_version",
+    "xp_send_recv_noalloc",
 ]
 
 
@@ -74,6 +75,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         "xp_status_string": [I],
         "xp_last_error": [],
         "xp_version": [],
+        "xp_send_recv_noalloc": [P, P, Z, I, I, Z, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -204,6 +206,13 @@ def xp_set_spin_timeout_ns(ns: int) -> None:
 
 def xp_abort(value: int) -> None:
     _check(_lib.xp_abort(value), "xp_abort")
+
+
+def xp_send_recv_noalloc(src, dst, nbytes: int, nchannels: int, nslots: int, slot_bytes: int,
+                         dev_status=None, stream=None) -> None:
+    """SIMPLE transfer through the library's static FIFO: allocates nothing."""
+    _check(_lib.xp_send_recv_noalloc(_ptr(src), _ptr(dst), nbytes, nchannels, nslots, slot_bytes, _ptr(dev_status),
+                                     _stream(stream)), "xp_send_recv_noalloc")
 
 
 def library_path() -> str:

@@ -210,6 +210,30 @@ xp_status xp_ring_allreduce_virtual(xp_ring* r, const void* const* send_bufs, vo
 xp_status xp_ring_status(xp_ring* r, int sync, xp_report* report);
 xp_status xp_ring_reset(xp_ring* r);
 
+/* SIMPLE transfer that allocates nothing.  The pages have no counterpart:
+ * it exists for callers that must not allocate device memory while they run,
+ * e.g. code inside a memory-pool or allocator hook (cudaMalloc there could
+ * re-enter the allocator) or under a hard device-memory budget.  The caller
+ * passes src and dst as for xp_send_recv; the FIFO (control blocks, slots,
+ * status) lives in one static device array of this library, 8 MiB of slots
+ * plus 16.25 KiB, that every GPU which loads the library keeps reserved until
+ * the process exits.  Limits: 1 <= nchannels <= 16, 1 <= nslots <= 64,
+ * slot_bytes a non-zero multiple of 16, and nchannels x
+ * round_up(nslots x slot_bytes, 4096) <= 8 MiB; larger FIFOs are refused with
+ * XP_ERR_INVALID and a message in xp_last_error().  One sender CTA and one
+ * receiver CTA per channel; the default 2 s spin timeout; the host abort
+ * word is not polled.  Each call clears the array's counters and status,
+ * launches one kernel on `stream` and, if dev_status (a device pointer) is
+ * not NULL, copies the device-side xp_status of the transfer there
+ * asynchronously.  All calls share the one array: calls whose transfers
+ * overlap in time on the GPU (other streams, other host threads) race and
+ * corrupt each other.  The first call on a device looks up the array's
+ * device address and sets a kernel attribute; make it before any stream
+ * capture.  Nothing here calls cudaMalloc, cudaFree or an allocating
+ * library routine. */
+xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t bytes, int nchannels, int nslots,
+                               size_t slot_bytes, int32_t* dev_status, xp_stream_t stream);
+
 /* Spin timeout of every device wait in later launches, in ns (default 2e9;
  * 1e3 <= ns <= 6e10). */
 xp_status xp_set_spin_timeout_ns(uint64_t ns);
