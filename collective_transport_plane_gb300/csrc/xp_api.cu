@@ -23,6 +23,9 @@ int p2p_tma_smem();
 void* ll_kernel_ptr();
 void* ll_pingpong_kernel_ptr();
 void* ring_kernel_ptr(int dtype);
+void* ring_tma_kernel_ptr(int dtype);
+int ring_tma_threads();
+int ring_tma_smem();
 }  // namespace xp
 
 using xp::DevStatus;
@@ -534,7 +537,14 @@ xp_status xp_ring_allreduce_virtual(xp_ring* r, const void* const* send_bufs, vo
   p.timeout_ns = g_timeout_ns.load();
   const int csize = r->P * r->lanes;
   XP_CUDA(cudaMemsetAsync(r->cm.status, 0, xp::kStatusClearBytes, st));
-  if ((s = launch(xp::ring_kernel_ptr(dt), r->C * csize, xp::kRingThreads, csize, &p, st)) != XP_OK) return s;
+  if (r->place == XP_PLACE_DEVICE) {
+    // HBM FIFOs: bulk copies through shared memory
+    s = launch(xp::ring_tma_kernel_ptr(dt), r->C * csize, xp::ring_tma_threads(), csize, &p, st, xp::ring_tma_smem());
+  } else {
+    // mapped host FIFOs: 16-byte vector loads and stores from every warp
+    s = launch(xp::ring_kernel_ptr(dt), r->C * csize, xp::kRingThreads, csize, &p, st);
+  }
+  if (s != XP_OK) return s;
   XP_CUDA(cudaEventRecord(r->cm.done, st));
   r->cm.used = true;
   return XP_OK;
