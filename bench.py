@@ -121,6 +121,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(ms: float) -> float:
+    """The slowest rank's time (replicas run in lock step between barriers)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, nbytes: int, steps: int, total_ms: float) -> float:
+    """Payload of every rank's steps over the slowest rank's time, in GB/s."""
+    return world * nbytes * steps / (total_ms * 1e-3) / 1e9
+
+
 def time_events(torch, stream, fn, iters):
     """Per-iteration device times (ms) with CUDA events on `stream`."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
@@ -257,13 +273,9 @@ def main():
     st, rep = xp.xp_fifo_status(fifo, True)
     if st != xp.XP_OK:
         raise RuntimeError(f"timed transfer failed: status {st}")
-    total_ms = sum(per)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per))
     ms_step = total_ms / args.steps
-    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, nbytes, args.steps, total_ms)
     avg_launch_ms = statistics.mean(per)
     achieved = 4 * nbytes / (avg_launch_ms * 1e-3) / 1e9
 
@@ -453,7 +465,7 @@ def rows(torch, xp, hbm_peak):
     xs = [torch.from_numpy(x).to("cuda") for x in workloads.ring_inputs(wr["nranks"], wr["nelems"], "f32", wr["seed_base"])]
     ys = [torch.empty_like(x) for x in xs]
     ring = {}
-    for lanes in (1, 2):
+    for lanes in (1,):
         r = xp.xp_ring_create(wr["nranks"], wr["nchannels"], wr["nslots"], wr["slot_bytes"])
         try:
             xp.xp_ring_set_lanes(r, lanes)

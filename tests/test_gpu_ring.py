@@ -93,3 +93,13 @@ def test_ring_workload(env, dtype):
     want = oracle.ring_order_sum(xs, w["nchannels"], w["nslots"], w["slot_bytes"])
     for got in _ring(torch, xp, xs, w["nchannels"], w["nslots"], w["slot_bytes"]):
         assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_ring_host_placed(env, dtype):
+    # FIFOs in mapped host memory: the vector-copy ring kernel
+    torch, xp = env
+    xs = _inputs(4, 100003, dtype, seed_base=3)
+    want = oracle.ring_order_sum(xs, 3, 4, 4096)
+    for got in _ring(torch, xp, xs, 3, 4, 4096, place=xp.XP_PLACE_HOST_MAPPED):
+        assert np.array_equal(got, want)

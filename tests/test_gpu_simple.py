@@ -177,3 +177,13 @@ def test_argument_errors(env):
         xp.xp_fifo_set_lanes(ll, 2)
     xp.xp_fifo_destroy(ll)
     xp.xp_fifo_destroy(fifo)
+
+
+@pytest.mark.parametrize("lanes", [1, 2])
+def test_zero_copy_host_placed(env, lanes):
+    # control block (ptrExchange, head, tail) in mapped host memory
+    torch, xp = env
+    src = workloads.uniform_bytes(300007, seed=12)
+    want, _, _ = oracle.zero_copy_transfer(src, 3, 2, 4096, seed=6)
+    got, _ = _run_simple(torch, xp, src, 3, 2, 4096, lanes=lanes, place=xp.XP_PLACE_HOST_MAPPED, zero_copy=True)
+    assert np.array_equal(got, want)
