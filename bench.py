@@ -215,7 +215,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--lanes", type=int, default=6)
+    ap.add_argument("--lanes", type=int, default=6, help="sender CTAs per channel")
+    ap.add_argument("--rlanes", type=int, default=7, help="receiver CTAs per channel")
     ap.add_argument("--no-rows", action="store_true", help="time the step only")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--mib", type=int, default=0,
@@ -247,6 +248,7 @@ def main():
     stream = torch.cuda.Stream()
     fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
     xp.xp_fifo_set_lanes(fifo, args.lanes)
+    xp.xp_fifo_set_recv_lanes(fifo, args.rlanes)
 
     def step():
         xp.xp_send_recv(fifo, src, dst, nbytes, stream)
@@ -285,7 +287,8 @@ def main():
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": "SIMPLE multi-channel: 1 GiB bf16 N(0,1) seed 2, 16 channels x 8 slots x 512 KiB, FIFO in HBM",
                    "nchannels": w["nchannels"], "nslots": w["nslots"], "slot_bytes": w["slot_bytes"],
-                   "lanes_per_side": args.lanes, "payload_bytes": nbytes, "parallelism": f"replicas{world}",
+                   "sender_ctas_per_channel": args.lanes, "receiver_ctas_per_channel": args.rlanes,
+                   "payload_bytes": nbytes, "parallelism": f"replicas{world}",
                    "l2": "inputs (1 GiB) larger than L2; the 64 MiB FIFO itself is L2-resident by design"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",

@@ -228,7 +228,8 @@ struct xp_fifo {
   size_t S = 0;
   xp_proto proto = XP_PROTO_SIMPLE;
   xp_placement place = XP_PLACE_DEVICE;
-  int lanes = 1;
+  int lanes = 1;           // sender CTAs per channel
+  int rlanes = 1;          // receiver CTAs per channel
   Mem mem;
   char* ctl = nullptr;     // device view
   char* slots = nullptr;   // device view
@@ -328,6 +329,16 @@ xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes) {
   if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
   if (lanes < 1 || lanes > 8) return fail(XP_ERR_INVALID, "lanes %d not in [1, 8]", lanes);
   f->lanes = lanes;
+  f->rlanes = lanes;
+  return XP_OK;
+}
+
+xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
+  if (rlanes < 1 || f->lanes + rlanes > xp::kMaxCluster)
+    return fail(XP_ERR_INVALID, "receiver lanes %d: need 1 <= rlanes and lanes + rlanes <= 16", rlanes);
+  f->rlanes = rlanes;
   return XP_OK;
 }
 
@@ -341,6 +352,7 @@ xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out) 
   out->proto = f->proto;
   out->placement = f->place;
   out->lanes = f->lanes;
+  out->recv_lanes = f->rlanes;
   return XP_OK;
 }
 
@@ -378,7 +390,8 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     block = xp::kLLThreads;
   } else {
     p.lanes = f->lanes;
-    csize = zero_copy ? f->lanes + 1 : 2 * f->lanes;
+    p.rlanes = zero_copy ? 1 : f->rlanes;
+    csize = p.lanes + p.rlanes;
     if (f->place == XP_PLACE_DEVICE) {
       // HBM FIFO: bulk copies through shared memory
       kernel = xp::p2p_tma_kernel_ptr(zero_copy);

@@ -55,7 +55,8 @@ struct P2pParams {
   unsigned long long nbytes;
   int nchannels;
   int nslots;
-  int lanes;                      // CTAs per side per channel
+  int lanes;                      // sender CTAs per channel
+  int rlanes;                     // receiver CTAs per channel (SIMPLE, HBM FIFO)
   int csize;                      // cluster size
   unsigned int slot_bytes;
   DevStatus* status;

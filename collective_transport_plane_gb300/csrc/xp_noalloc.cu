@@ -108,6 +108,7 @@ extern "C" xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t byt
   p.nchannels = nchannels;
   p.nslots = nslots;
   p.lanes = 1;
+  p.rlanes = 1;
   p.csize = 2;
   p.slot_bytes = (unsigned)slot_bytes;
   p.status = status;

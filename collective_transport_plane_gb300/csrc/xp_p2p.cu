@@ -1,8 +1,8 @@
 // SIMPLE and zero-copy channel kernels.
 //
 // One thread-block cluster per channel.  SIMPLE: CTAs [0, G) are the sender
-// lanes and [G, 2G) the receiver lanes; zero copy: [0, G) senders and CTA G
-// the receiver.  Every CTA has kCopyWarps copy warps and one publisher warp.
+// lanes and [G, G + GR) the receiver lanes; zero copy: [0, G) senders and
+// CTA G the receiver.  Every CTA has kCopyWarps copy warps and one publisher warp.
 // Each slot-step is split into G*kCopyWarps contiguous 16-byte-vector pieces,
 // one per copy warp of the side; a warp that finished its piece arrives
 // (release, cluster scope) on the slot's mbarrier in the side's leader CTA
@@ -39,10 +39,11 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
   const int lane = threadIdx.x & 31;
   const unsigned crank = cluster_ctarank();
   const int ch = blockIdx.x / p.csize;
-  const int G = p.lanes;
+  const int G = p.lanes;                          // sender lanes
   const bool sender = crank < (unsigned)G;
   const int lane_id = sender ? (int)crank : (int)crank - G;
   const unsigned leader = sender ? 0u : (unsigned)G;
+  const int GS = (sender || kZeroCopy) ? G : p.rlanes;   // lanes of this CTA's side
   const bool leader_cta = crank == leader;
   const u64 N = (u64)p.nslots;
   const u64 S = p.slot_bytes;
@@ -65,7 +66,7 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
     s_base = ld_relaxed(basew);
     s_stop = sticky_stop(w) ? 1 : 0;
     if (leader_cta) {
-      const uint32_t count = (uint32_t)(G * kCopyWarps);
+      const uint32_t count = (uint32_t)(GS * kCopyWarps);
       for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), count);
       mbar_init_fence();
     }
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
   const bool run = nsteps > 0 && s_stop == 0;
 
   if (run && warp < kCopyWarps) {
-    const u64 parts = (u64)G * kCopyWarps;
+    const u64 parts = (u64)GS * kCopyWarps;
     const u64 my_piece = (u64)lane_id * kCopyWarps + warp;
     const uint32_t bar0 = map_to_rank(smem_addr(&bars[0]), leader);
     if (sender) {

@@ -2,7 +2,7 @@
 // (TMA) copies through shared memory.
 //
 // Cluster layout as in the vector kernels (xp_p2p.cu): per channel, CTAs
-// [0, G) send and [G, 2G) receive (zero copy: CTA G receives).  Each CTA moves
+// [0, G) send and [G, G + GR) receive (zero copy: CTA G receives).  Each CTA moves
 // one contiguous stripe of every slot-step ("lane") through a ring of
 // kTmaStages shared-memory stages:
 //   sender    - one mover thread issues bulk loads from src up to kLookSend
@@ -122,9 +122,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   const int lane = threadIdx.x & 31;
   const unsigned crank = cluster_ctarank();
   const int ch = blockIdx.x / p.csize;
-  const int G = p.lanes;
+  const int G = p.lanes;                        // sender lanes
+  const int GR = kZeroCopy ? 1 : p.rlanes;      // receiver lanes
   const bool sender = crank < (unsigned)G;
   const int lane_id = sender ? (int)crank : (int)crank - G;
+  const int GS = sender ? G : GR;               // lanes of this CTA's side
   const unsigned leader = sender ? 0u : (unsigned)G;
   const bool leader_cta = crank == leader;
   const u64 N = (u64)p.nslots;
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       mbar_init(smem_addr(&empty[k]), 1);
     }
     if (leader_cta)
-      for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), (uint32_t)G);
+      for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), (uint32_t)GS);
     mbar_init_fence();
   }
   cluster_sync_all();
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       }
     } else if (warp == 0) {
       Entries en;
-      en.init(len, S, (u64)G, (u64)lane_id);
+      en.init(len, S, (u64)GS, (u64)lane_id);
       const u64 total = en.total;
       u64 jl = 0;   // next entry to load
       u64 j = 0;    // next entry to store
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       // stores each loaded entry into dst; once the last entry of a step is
       // in shared memory the stripe of the slot has been read: signal it
       Entries en;
-      en.init(len, S, (u64)G, (u64)lane_id);
+      en.init(len, S, (u64)GS, (u64)lane_id);
       u64 j = 0;
       bool ok = true;
       for (u64 s = 0; s < nsteps && ok; ++s) {

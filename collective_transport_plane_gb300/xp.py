@@ -27,7 +27,7 @@ EXPORTS = [
     "xp_send_recv_zero_copy", "xp_fifo_status", "xp_fifo_reset", "xp_ll_pingpong", "xp_ring_create",
     "xp_ring_destroy", "xp_ring_set_lanes", "xp_ring_allreduce_virtual", "xp_ring_status", "xp_ring_reset",
     "xp_set_spin_timeout_ns", "xp_abort", "xp_status_string", "xp_last_error", "xp_version",
-    "xp_send_recv_noalloc",
+    "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes",
 ]
 
 
@@ -40,7 +40,7 @@ class xp_report(ctypes.Structure):
 class xp_channel_desc(ctypes.Structure):
     _fields_ = [("ctl", ctypes.c_void_p), ("slots", ctypes.c_void_p), ("slot_stride", ctypes.c_size_t),
                 ("nslots", ctypes.c_int), ("proto", ctypes.c_int), ("placement", ctypes.c_int),
-                ("lanes", ctypes.c_int)]
+                ("lanes", ctypes.c_int), ("recv_lanes", ctypes.c_int)]
 
 
 class XpError(RuntimeError):
@@ -58,6 +58,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         "xp_fifo_create": [I, I, Z, I, I, ctypes.POINTER(P)],
         "xp_fifo_destroy": [P],
         "xp_fifo_set_lanes": [P, I],
+        "xp_fifo_set_recv_lanes": [P, I],
         "xp_fifo_describe": [P, I, ctypes.POINTER(xp_channel_desc)],
         "xp_send_recv": [P, P, P, Z, P],
         "xp_send_recv_zero_copy": [P, P, P, Z, P],
@@ -135,6 +136,10 @@ def xp_fifo_destroy(fifo: int) -> None:
 
 def xp_fifo_set_lanes(fifo: int, lanes: int) -> None:
     _check(_lib.xp_fifo_set_lanes(fifo, lanes), "xp_fifo_set_lanes")
+
+
+def xp_fifo_set_recv_lanes(fifo: int, rlanes: int) -> None:
+    _check(_lib.xp_fifo_set_recv_lanes(fifo, rlanes), "xp_fifo_set_recv_lanes")
 
 
 def xp_fifo_describe(fifo: int, channel: int) -> xp_channel_desc:

@@ -112,7 +112,8 @@ typedef struct {
   int nslots;
   int proto;
   int placement;
-  int lanes;
+  int lanes;          /* sender CTAs per channel   */
+  int recv_lanes;     /* receiver CTAs per channel */
 } xp_channel_desc;
 
 /* Create a FIFO of `nchannels` independent channels, each with `nslots`
@@ -134,9 +135,15 @@ xp_status xp_fifo_destroy(xp_fifo* f);
 /* CTAs per channel side: each channel's sender and receiver are each spread
  * over `lanes` CTAs of one thread-block cluster that share the channel's one
  * tail and one head (1 <= lanes <= 8; default 1: one sender CTA and one
- * receiver CTA per channel).  SIMPLE FIFOs only.  Takes effect at the next
- * operation. */
+ * receiver CTA per channel).  Sets both sides.  SIMPLE FIFOs only.  Takes
+ * effect at the next operation. */
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
+
+/* Receiver CTAs per channel of xp_send_recv, independently of the sender's
+ * (1 <= rlanes, lanes + rlanes <= 16): the slot-step is published whole, so
+ * the receiver may cut it into a different number of stripes.  Zero copy
+ * always uses one receiver CTA.  SIMPLE FIFOs only. */
+xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes);
 
 /* Channel layout (pointers stay valid until destroy). */
 xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out);

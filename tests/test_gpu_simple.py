@@ -187,3 +187,22 @@ def test_zero_copy_host_placed(env, lanes):
     want, _, _ = oracle.zero_copy_transfer(src, 3, 2, 4096, seed=6)
     got, _ = _run_simple(torch, xp, src, 3, 2, 4096, lanes=lanes, place=xp.XP_PLACE_HOST_MAPPED, zero_copy=True)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("n,nchan,nslots,slot,lanes,rlanes,place", [
+    (1000003, 3, 4, 65536, 2, 5, 0), (777777, 16, 2, 16384, 6, 7, 0), (65537, 2, 1, 4096, 3, 1, 0),
+    (300007, 4, 2, 8192, 1, 3, 1), (1 << 20, 2, 8, 65536, 3, 2, 1)])
+def test_simple_receiver_lanes(env, n, nchan, nslots, slot, lanes, rlanes, place):
+    # the receiver cuts each published slot-step into its own number of stripes
+    torch, xp = env
+    src = workloads.uniform_bytes(n, seed=n % 91)
+    want, _, _ = oracle.simple_transfer(src, nchan, nslots, slot, seed=7)
+    fifo = xp.xp_fifo_create(nchan, nslots, slot, xp.XP_PROTO_SIMPLE, place)
+    xp.xp_fifo_set_lanes(fifo, lanes)
+    xp.xp_fifo_set_recv_lanes(fifo, rlanes)
+    d = xp.xp_fifo_describe(fifo, 0)
+    assert (d.lanes, d.recv_lanes) == (lanes, rlanes)
+    for _ in range(2):
+        got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, fifo=fifo)
+        assert np.array_equal(got, want)
+    xp.xp_fifo_destroy(fifo)
