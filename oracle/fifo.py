@@ -565,6 +565,160 @@ class ZeroCopySender(Actor):
 
 
 # --------------------------------------------------------------------------
+# Receiver-driven credit FIFO ("RDMA and GPUDirect" §4.3; "NCCL transport
+# data transfer (二)", netTransport stage 2)
+# --------------------------------------------------------------------------
+
+@dataclass
+class Post:
+    """One receiver post: where chunk `idx - 1` must land."""
+    buf: np.ndarray
+    offset: int
+    size: int
+    idx: int
+    taken: bool = False
+
+
+class PostedChannel:
+    """The sender-side FIFO of N posts and the receiver-side completion queue.
+
+    The receiver owns credit: it never has more than N posts outstanding
+    (posted but not completed).  A post for chunk j carries idx = base + j + 1
+    (the pages' first index is 1 after a head of 0), so a slot holding an older
+    post never matches."""
+
+    def __init__(self, nslots: int, slot_bytes: int, step0: int = 0):
+        self.N = nslots
+        self.S = slot_bytes
+        self.posts: list[Post | None] = [None] * nslots
+        self.cq: list[tuple[int, int] | None] = [None] * nslots   # (idx, size)
+        self.base = step0
+        self.posted = step0          # posts written (absolute chunk count)
+        self.completed = step0       # completions consumed by the receiver
+        self.max_outstanding = 0
+
+    def check(self):
+        out = self.posted - self.completed
+        if out < 0 or out > self.N:
+            raise ProtocolViolation(f"{out} posts outstanding with N {self.N}")
+        self.max_outstanding = max(self.max_outstanding, out)
+
+    def state(self):
+        return (self.posted, self.completed,
+                tuple(None if q is None else (q.offset, q.size, q.idx, q.taken) for q in self.posts),
+                tuple(self.cq))
+
+
+class PostedReceiver(Actor):
+    """Post chunk j's destination while fewer than N posts are outstanding;
+    consume completions in order, checking the size each reports.
+    `fault`: "overpost" (ignores the N limit)."""
+
+    def __init__(self, ch: PostedChannel, dst: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.c, self.dst, self.lo, self.hi = ch, dst, lo, hi
+        self.base = ch.completed
+        self.nchunks = ceil_div(hi - lo, ch.S)
+        self.next_post = 0
+        self.next_done = 0
+        self.fault = fault
+        self.name = f"posted-recv[{lo}:{hi}]"
+
+    def done(self):
+        return self.next_done >= self.nchunks
+
+    def _size(self, j):
+        return min(self.c.S, self.hi - self.lo - j * self.c.S)
+
+    def choices(self):
+        if self.done():
+            return []
+        opts = []
+        limit = self.next_done + (self.nchunks if self.fault == "overpost" else self.c.N)
+        if self.next_post < self.nchunks and self.next_post < limit:
+            opts.append(("post",))
+        q = self.c.cq[(self.base + self.next_done) % self.c.N]
+        if q is not None and q[0] == self.base + self.next_done + 1:
+            opts.append(("complete",))
+        return opts
+
+    def fire(self, choice):
+        if choice[0] == "post":
+            j = self.next_post
+            k = (self.base + j) % self.c.N
+            old = self.c.posts[k]
+            if old is not None and not old.taken and self.fault != "overpost":
+                raise ProtocolViolation(f"post {j} overwrites untaken post idx {old.idx}")
+            self.c.posts[k] = Post(self.dst, self.lo + j * self.c.S, self._size(j), self.base + j + 1)
+            self.next_post += 1
+            self.c.posted = self.base + self.next_post
+        else:
+            j = self.next_done
+            idx, size = self.c.cq[(self.base + j) % self.c.N]
+            if size != self._size(j):
+                raise ProtocolViolation(f"completion of chunk {j} reports {size} bytes, expected {self._size(j)}")
+            self.next_done += 1
+            self.c.completed = self.base + self.next_done
+
+    def state(self):
+        return (self.next_post, self.next_done)
+
+
+class PostedSender(Actor):
+    """For chunk j: wait for the post with idx base + j + 1, write the chunk
+    at its address, write the completion {idx, size}.
+    `fault`: "ignore_idx" (takes whatever post is in the slot)."""
+    WAIT, COPY, COMPLETE, DONE = range(4)
+
+    def __init__(self, ch: PostedChannel, src: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.c, self.src, self.lo, self.hi = ch, src, lo, hi
+        self.base = ch.completed
+        self.nchunks = ceil_div(hi - lo, ch.S)
+        self.j = 0
+        self.post: Post | None = None
+        self.phase = self.WAIT if self.nchunks else self.DONE
+        self.fault = fault
+        self.name = f"posted-send[{lo}:{hi}]"
+
+    def done(self):
+        return self.phase == self.DONE
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT:
+            q = self.c.posts[(self.base + self.j) % self.c.N]
+            ok = q is not None and (self.fault == "ignore_idx" or q.idx == self.base + self.j + 1)
+            return [0] if ok else []
+        return [0]
+
+    def fire(self, choice):
+        if self.phase == self.WAIT:
+            q = self.c.posts[(self.base + self.j) % self.c.N]
+            if q.taken:
+                raise ProtocolViolation(f"post idx {q.idx} consumed twice")
+            if q.idx != self.base + self.j + 1:
+                raise ProtocolViolation(f"chunk {self.j} took post idx {q.idx}")
+            q.taken = True
+            self.post = q
+            self.phase = self.COPY
+        elif self.phase == self.COPY:
+            off = self.lo + self.j * self.c.S
+            n = min(self.c.S, self.hi - off)
+            if n > self.post.size:
+                raise ProtocolViolation(f"chunk of {n} bytes into a post of {self.post.size}")
+            self.post.buf[self.post.offset:self.post.offset + n] = self.src[off:off + n]
+            self.phase = self.COMPLETE
+        else:
+            n = min(self.c.S, self.hi - self.lo - self.j * self.c.S)
+            self.c.cq[(self.base + self.j) % self.c.N] = (self.base + self.j + 1, n)
+            self.j += 1
+            self.phase = self.WAIT if self.j < self.nchunks else self.DONE
+
+    def state(self):
+        return (self.j, self.phase)
+
+
+# --------------------------------------------------------------------------
 # Schedulers
 # --------------------------------------------------------------------------
 

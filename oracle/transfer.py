@@ -10,8 +10,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from .fifo import (LLFifo, LLReceiver, LLSender, SimpleFifo, SimpleReceiver, SimpleSender, System,
-                   ZeroCopyChannel, ZeroCopyReceiver, ZeroCopySender, run)
+from .fifo import (LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender, SimpleFifo,
+                   SimpleReceiver, SimpleSender, System, ZeroCopyChannel, ZeroCopyReceiver, ZeroCopySender, run)
 from .partition import channel_byte_ranges
 from .ring import ring_system
 
@@ -59,6 +59,21 @@ def zero_copy_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes:
     for c, (lo, hi) in zip(chans, channel_byte_ranges(len(src), nchannels)):
         if hi > lo:
             actors += [ZeroCopySender(c, src, lo, hi), ZeroCopyReceiver(c, dst, lo, hi)]
+    ev = run(System(actors, chans, [dst]), seed=seed)
+    return dst, chans, ev
+
+
+def posted_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: int, seed: int = 0,
+                    chans: list[PostedChannel] | None = None):
+    """Receiver-driven credit transfer of the byte buffer `src`; returns (dst, channels, events)."""
+    src = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
+    dst = np.zeros_like(src)
+    if chans is None:
+        chans = [PostedChannel(nslots, slot_bytes) for _ in range(nchannels)]
+    actors = []
+    for c, (lo, hi) in zip(chans, channel_byte_ranges(len(src), nchannels)):
+        if hi > lo:
+            actors += [PostedSender(c, src, lo, hi), PostedReceiver(c, dst, lo, hi)]
     ev = run(System(actors, chans, [dst]), seed=seed)
     return dst, chans, ev
 
