@@ -565,13 +565,14 @@ class ZeroCopySender(Actor):
 
 
 # --------------------------------------------------------------------------
-# Receiver-driven credit FIFO ("RDMA and GPUDirect" §4.3; "NCCL transport
-# data transfer (二)", netTransport stage 2)
+# Receiver-driven credit FIFO ("RDMA and GPUDirect" §4.3, the sender FIFO;
+# "NCCL transport data transfer (二)", netTransport copy and zero-copy modes)
 # --------------------------------------------------------------------------
 
 @dataclass
 class Post:
-    """One receiver post: where chunk `idx - 1` must land."""
+    """One receiver post: chunk `idx - base - 1` may be written to
+    buf[offset : offset + size]."""
     buf: np.ndarray
     offset: int
     size: int
@@ -580,21 +581,23 @@ class Post:
 
 
 class PostedChannel:
-    """The sender-side FIFO of N posts and the receiver-side completion queue.
+    """The sender-side FIFO of N posts, the receiver-side completion queue and
+    the receiver's N staging slots of S bytes.
 
     The receiver owns credit: it never has more than N posts outstanding
-    (posted but not completed).  A post for chunk j carries idx = base + j + 1
-    (the pages' first index is 1 after a head of 0), so a slot holding an older
-    post never matches."""
+    (posted but not completed).  A post for chunk j of an operation carries
+    idx = base + j + 1 (the pages' first index is 1 after a head of 0), so a
+    FIFO entry left from an older post never matches.  `base` counts every
+    chunk of earlier operations on the channel."""
 
     def __init__(self, nslots: int, slot_bytes: int, step0: int = 0):
         self.N = nslots
         self.S = slot_bytes
+        self.slots = np.zeros(nslots * slot_bytes, np.uint8)
         self.posts: list[Post | None] = [None] * nslots
         self.cq: list[tuple[int, int] | None] = [None] * nslots   # (idx, size)
-        self.base = step0
         self.posted = step0          # posts written (absolute chunk count)
-        self.completed = step0       # completions consumed by the receiver
+        self.completed = step0       # chunks whose completion the receiver has consumed
         self.max_outstanding = 0
 
     def check(self):
@@ -606,25 +609,31 @@ class PostedChannel:
     def state(self):
         return (self.posted, self.completed,
                 tuple(None if q is None else (q.offset, q.size, q.idx, q.taken) for q in self.posts),
-                tuple(self.cq))
+                tuple(self.cq), self.slots.tobytes())
 
 
 class PostedReceiver(Actor):
-    """Post chunk j's destination while fewer than N posts are outstanding;
-    consume completions in order, checking the size each reports.
-    `fault`: "overpost" (ignores the N limit)."""
+    """Posts chunk j's landing place while fewer than N posts are outstanding,
+    consumes completions in order and checks the size each one reports.
 
-    def __init__(self, ch: PostedChannel, dst: np.ndarray, lo: int, hi: int, fault: str | None = None):
-        self.c, self.dst, self.lo, self.hi = ch, dst, lo, hi
+    direct=False (copy mode): the post names staging slot (base + j) mod N of
+    S bytes; after the completion the receiver copies the slot to dst and only
+    then counts the chunk consumed, which frees the slot for a new post.
+    direct=True (zero copy): the post names dst itself, exactly the chunk's
+    size.
+    `fault`: "overpost" (ignores the N limit), "early_free" (copy mode: counts
+    the chunk consumed before copying the slot out)."""
+
+    def __init__(self, ch: PostedChannel, dst: np.ndarray, lo: int, hi: int, direct: bool = False,
+                 fault: str | None = None):
+        self.c, self.dst, self.lo, self.hi, self.direct = ch, dst, lo, hi, direct
         self.base = ch.completed
         self.nchunks = ceil_div(hi - lo, ch.S)
         self.next_post = 0
         self.next_done = 0
+        self.landed = False          # copy mode: completion of next_done seen, slot not yet copied
         self.fault = fault
         self.name = f"posted-recv[{lo}:{hi}]"
-
-    def done(self):
-        return self.next_done >= self.nchunks
 
     def _size(self, j):
         return min(self.c.S, self.hi - self.lo - j * self.c.S)
@@ -636,37 +645,66 @@ class PostedReceiver(Actor):
         limit = self.next_done + (self.nchunks if self.fault == "overpost" else self.c.N)
         if self.next_post < self.nchunks and self.next_post < limit:
             opts.append(("post",))
-        q = self.c.cq[(self.base + self.next_done) % self.c.N]
-        if q is not None and q[0] == self.base + self.next_done + 1:
-            opts.append(("complete",))
+        if self.landed:
+            opts.append(("copy",))
+        else:
+            q = self.c.cq[(self.base + self.next_done) % self.c.N]
+            if q is not None and q[0] == self.base + self.next_done + 1:
+                opts.append(("complete",))
         return opts
 
     def fire(self, choice):
+        N, S = self.c.N, self.c.S
         if choice[0] == "post":
             j = self.next_post
-            k = (self.base + j) % self.c.N
+            k = (self.base + j) % N
             old = self.c.posts[k]
-            if old is not None and not old.taken and self.fault != "overpost":
+            if old is not None and not old.taken:
                 raise ProtocolViolation(f"post {j} overwrites untaken post idx {old.idx}")
-            self.c.posts[k] = Post(self.dst, self.lo + j * self.c.S, self._size(j), self.base + j + 1)
+            if self.direct:
+                self.c.posts[k] = Post(self.dst, self.lo + j * S, self._size(j), self.base + j + 1)
+            else:
+                self.c.posts[k] = Post(self.c.slots, k * S, S, self.base + j + 1)
             self.next_post += 1
             self.c.posted = self.base + self.next_post
-        else:
+        elif choice[0] == "complete":
             j = self.next_done
-            idx, size = self.c.cq[(self.base + j) % self.c.N]
+            idx, size = self.c.cq[(self.base + j) % N]
             if size != self._size(j):
                 raise ProtocolViolation(f"completion of chunk {j} reports {size} bytes, expected {self._size(j)}")
-            self.next_done += 1
-            self.c.completed = self.base + self.next_done
+            if self.direct:
+                self._consumed()
+            else:
+                self.landed = True
+                if self.fault == "early_free":
+                    self.next_done += 1
+                    self.c.completed = self.base + self.next_done
+        else:
+            j = self.next_done - (1 if self.fault == "early_free" else 0)
+            k = (self.base + j) % N
+            n = self._size(j)
+            self.dst[self.lo + j * S:self.lo + j * S + n] = self.c.slots[k * S:k * S + n]
+            self.landed = False
+            if self.fault != "early_free":
+                self._consumed()
+
+    def _consumed(self):
+        self.next_done += 1
+        self.c.completed = self.base + self.next_done
+
+    def done(self):
+        return self.next_done >= self.nchunks and not self.landed
 
     def state(self):
-        return (self.next_post, self.next_done)
+        return (self.next_post, self.next_done, self.landed)
 
 
 class PostedSender(Actor):
-    """For chunk j: wait for the post with idx base + j + 1, write the chunk
-    at its address, write the completion {idx, size}.
-    `fault`: "ignore_idx" (takes whatever post is in the slot)."""
+    """For chunk j: wait for the post whose idx is base + j + 1, check that the
+    chunk fits its size, write the chunk at its address, then write the
+    completion {idx, size} (the pages' write-with-immediate, whose immediate
+    is the size).
+    `fault`: "ignore_idx" (takes whatever post is in the FIFO entry)."""
     WAIT, COPY, COMPLETE, DONE = range(4)
 
     def __init__(self, ch: PostedChannel, src: np.ndarray, lo: int, hi: int, fault: str | None = None):

@@ -64,8 +64,9 @@ def zero_copy_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes:
 
 
 def posted_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: int, seed: int = 0,
-                    chans: list[PostedChannel] | None = None):
-    """Receiver-driven credit transfer of the byte buffer `src`; returns (dst, channels, events)."""
+                    chans: list[PostedChannel] | None = None, direct: bool = False):
+    """Receiver-driven credit transfer of the byte buffer `src` (copy mode
+    through staging slots, or direct into dst); returns (dst, channels, events)."""
     src = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
     dst = np.zeros_like(src)
     if chans is None:
@@ -73,7 +74,7 @@ def posted_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: in
     actors = []
     for c, (lo, hi) in zip(chans, channel_byte_ranges(len(src), nchannels)):
         if hi > lo:
-            actors += [PostedSender(c, src, lo, hi), PostedReceiver(c, dst, lo, hi)]
+            actors += [PostedSender(c, src, lo, hi), PostedReceiver(c, dst, lo, hi, direct=direct)]
     ev = run(System(actors, chans, [dst]), seed=seed)
     return dst, chans, ev
 
