@@ -381,6 +381,29 @@ def rows(torch, xp, hbm_peak):
     ms = statistics.median(t)
     res["simple_lanes1"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "frac_of_hbm": 4 * n / (ms * 1e-3) / 1e9 / hbm_peak}
     xp.xp_fifo_destroy(f)
+
+    # receiver-driven credit (posts {addr, size, idx}): copy mode through the
+    # staging slots (4 bytes of HBM traffic per payload byte) and direct
+    # mode into dst (2 bytes per payload byte)
+    posted = {}
+    for direct, lanes, rl in ((False, 6, 7), (True, 8, None)):
+        f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
+        xp.xp_fifo_set_lanes(f, lanes)
+        if rl:
+            xp.xp_fifo_set_recv_lanes(f, rl)
+        dst.zero_()
+        with torch.cuda.stream(s):
+            for _ in range(5):
+                xp.xp_send_recv_posted(f, src, dst, n, direct, s)
+            t = time_events(torch, s, lambda: xp.xp_send_recv_posted(f, src, dst, n, direct, s), 50)
+        st, _ = xp.xp_fifo_status(f, True)
+        ms = statistics.median(t)
+        per = 2 if direct else 4
+        posted["direct" if direct else "copy"] = {
+            "lanes": lanes, "recv_lanes": rl or 1, "gbs": n / (ms * 1e-3) / 1e9, "ms": ms,
+            "frac_of_hbm": per * n / (ms * 1e-3) / 1e9 / hbm_peak, "exact": bool(st == xp.XP_OK and torch.equal(dst, src))}
+        xp.xp_fifo_destroy(f)
+    res["posted"] = posted
     del src, dst
 
     # SIMPLE loopback: 1 MiB, one sender CTA -> one receiver CTA, 8 x 64 KiB

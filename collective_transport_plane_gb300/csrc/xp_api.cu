@@ -17,7 +17,7 @@
 
 namespace xp {
 void* p2p_kernel_ptr(bool zero_copy);
-void* p2p_tma_kernel_ptr(bool zero_copy);
+void* p2p_tma_kernel_ptr(int mode);   // 0 SIMPLE, 1 zero copy, 2 posted copy, 3 posted direct
 int p2p_tma_threads();
 int p2p_tma_smem();
 void* ll_kernel_ptr();
@@ -215,6 +215,22 @@ xp_status launch(const void* kernel, int grid, int block, int csize, void* param
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Marks the object's last operation on `st`.  Inside a stream capture the
+// operation becomes a graph node and nothing is recorded (an event recorded
+// during capture cannot be waited on afterwards): the caller synchronises the
+// graph's replays before reading the status.
+xp_status record_done(Common& c, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cs = cudaStreamCaptureStatusNone;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return XP_OK;
+  XP_CUDA(cudaEventRecord(c.done, st));
+  c.used = true;
+  return XP_OK;
+}
+
 }  // namespace
 
 namespace xp {
@@ -233,7 +249,9 @@ struct xp_fifo {
   Mem mem;
   char* ctl = nullptr;     // device view
   char* slots = nullptr;   // device view
+  char* pctl = nullptr;    // device view: posted-FIFO blocks
   size_t ctl_region = 0;
+  size_t pctl_region = 0;
   size_t ch_stride = 0;
 };
 
@@ -301,8 +319,10 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
   f->proto = proto;
   f->place = place;
   f->ctl_region = round_up((size_t)nchannels * xp::kCtlBytes, 4096);
+  f->pctl_region = (size_t)nchannels * xp::kPostCtlBytes;
   f->ch_stride = round_up((size_t)nslots * slot_bytes, 4096);
-  if ((s = common_init(f->cm)) != XP_OK || (s = mem_alloc(f->mem, f->ctl_region + nchannels * f->ch_stride, place)) != XP_OK ||
+  if ((s = common_init(f->cm)) != XP_OK ||
+      (s = mem_alloc(f->mem, f->ctl_region + f->pctl_region + nchannels * f->ch_stride, place)) != XP_OK ||
       (s = mem_init(f->mem, nchannels)) != XP_OK) {
     common_free(f->cm);
     mem_free(f->mem);
@@ -310,7 +330,8 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
     return s;
   }
   f->ctl = f->mem.dev;
-  f->slots = f->mem.dev + f->ctl_region;
+  f->pctl = f->mem.dev + f->ctl_region;
+  f->slots = f->pctl + f->pctl_region;
   *out = f;
   return XP_OK;
 }
@@ -353,10 +374,15 @@ xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out) 
   out->placement = f->place;
   out->lanes = f->lanes;
   out->recv_lanes = f->rlanes;
+  out->posted = f->pctl + (size_t)channel * xp::kPostCtlBytes;
   return XP_OK;
 }
 
-static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream, bool zero_copy) {
+enum { kOpSimple = 0, kOpZeroCopy = 1, kOpPostedCopy = 2, kOpPostedDirect = 3 };   // p2p_tma_kernel_ptr modes
+
+static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream, int mode) {
+  const bool zero_copy = mode == kOpZeroCopy;
+  const bool posted = mode >= kOpPostedCopy;
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (bytes == 0) return XP_OK;
   if (!src || !dst) return fail(XP_ERR_INVALID, "src or dst is NULL");
@@ -364,12 +390,15 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
   if (s0 < d0 + bytes && d0 < s0 + bytes) return fail(XP_ERR_INVALID, "src and dst overlap");
   if (zero_copy && f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "zero copy needs a SIMPLE FIFO");
+  if (posted && (f->proto != XP_PROTO_SIMPLE || f->place != XP_PLACE_DEVICE))
+    return fail(XP_ERR_INVALID, "posted transfers need a SIMPLE FIFO in device memory");
   if (f->proto == XP_PROTO_LL && bytes % 8) return fail(XP_ERR_INVALID, "LL moves whole 8-byte lines: bytes %% 8 != 0");
   xp_status s = check_device(f->cm);
   if (s != XP_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   xp::P2pParams p = {};
   p.ctl = f->ctl;
+  p.pctl = f->pctl;
   p.slots = f->slots;
   p.ch_stride = f->ch_stride;
   p.src = static_cast<const char*>(src);
@@ -390,11 +419,11 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     block = xp::kLLThreads;
   } else {
     p.lanes = f->lanes;
-    p.rlanes = zero_copy ? 1 : f->rlanes;
+    p.rlanes = (zero_copy || mode == kOpPostedDirect) ? 1 : f->rlanes;
     csize = p.lanes + p.rlanes;
     if (f->place == XP_PLACE_DEVICE) {
       // HBM FIFO: bulk copies through shared memory
-      kernel = xp::p2p_tma_kernel_ptr(zero_copy);
+      kernel = xp::p2p_tma_kernel_ptr(mode);
       block = xp::p2p_tma_threads();
       smem = xp::p2p_tma_smem();
     } else {
@@ -406,17 +435,19 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   p.csize = csize;
   XP_CUDA(cudaMemsetAsync(f->cm.status, 0, xp::kStatusClearBytes, st));
   if ((s = launch(kernel, f->C * csize, block, csize, &p, st, smem)) != XP_OK) return s;
-  XP_CUDA(cudaEventRecord(f->cm.done, st));
-  f->cm.used = true;
-  return XP_OK;
+  return record_done(f->cm, st);
 }
 
 xp_status xp_send_recv(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream) {
-  return p2p_op(f, src, dst, bytes, stream, false);
+  return p2p_op(f, src, dst, bytes, stream, kOpSimple);
 }
 
 xp_status xp_send_recv_zero_copy(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream) {
-  return p2p_op(f, src, dst, bytes, stream, true);
+  return p2p_op(f, src, dst, bytes, stream, kOpZeroCopy);
+}
+
+xp_status xp_send_recv_posted(xp_fifo* f, const void* src, void* dst, size_t bytes, int direct, xp_stream_t stream) {
+  return p2p_op(f, src, dst, bytes, stream, direct ? kOpPostedDirect : kOpPostedCopy);
 }
 
 xp_status xp_fifo_status(xp_fifo* f, int sync, xp_report* report) {
@@ -558,9 +589,7 @@ xp_status xp_ring_allreduce_virtual(xp_ring* r, const void* const* send_bufs, vo
     s = launch(xp::ring_kernel_ptr(dt), r->C * csize, xp::kRingThreads, csize, &p, st);
   }
   if (s != XP_OK) return s;
-  XP_CUDA(cudaEventRecord(r->cm.done, st));
-  r->cm.used = true;
-  return XP_OK;
+  return record_done(r->cm, st);
 }
 
 xp_status xp_ring_status(xp_ring* r, int sync, xp_report* report) {

@@ -23,6 +23,16 @@ constexpr int kPtrxOff = 256;   // ptrExchange: receiver's destination for zero 
 constexpr int kBaseOff = 384;   // first step of the next operation (device-side epoch)
 constexpr int kSizeOff = 512;   // int64 size word per slot, -1 = never written
 
+// Per-channel block of the receiver-driven credit FIFO (posted transfers):
+// kMaxSlots post entries of 64 bytes {addr, size, idx, pad}, written by the
+// receiver and read by the sender; kMaxSlots completion entries of 16 bytes
+// {size, idx}, written by the sender; and the step base of the next posted
+// operation on its own line.
+constexpr int kPostCtlBytes = 8192;
+constexpr int kPostOff = 0;
+constexpr int kComplOff = 64 * kMaxSlots;
+constexpr int kPostBaseOff = kComplOff + 16 * kMaxSlots;
+
 constexpr int kCopyWarps = 16;                  // data-moving warps per CTA
 constexpr int kP2pThreads = 32 * (kCopyWarps + 1);   // + 1 publisher warp
 constexpr int kRingThreads = 32 * (kCopyWarps + 2);  // + tail and head publishers
@@ -48,6 +58,7 @@ constexpr int kStatusClearBytes = 64;
 
 struct P2pParams {
   char* ctl;                      // nchannels control blocks
+  char* pctl;                     // nchannels posted-FIFO blocks (posted transfers)
   char* slots;                    // channel c's slot k at slots + c*ch_stride + k*slot_bytes
   unsigned long long ch_stride;
   const char* src;

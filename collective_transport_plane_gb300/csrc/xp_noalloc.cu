@@ -17,7 +17,7 @@
 
 namespace xp {
 void set_last_error(const char* msg);
-void* p2p_tma_kernel_ptr(bool zero_copy);
+void* p2p_tma_kernel_ptr(int mode);
 int p2p_tma_threads();
 int p2p_tma_smem();
 }  // namespace xp
@@ -85,7 +85,7 @@ extern "C" xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t byt
       void* ptr = nullptr;
       if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess) return cuda_failed("cudaGetSymbolAddress", e);
       if (!ptr) return invalid("xp_send_recv_noalloc: no device address for the static FIFO");
-      const void* kern = xp::p2p_tma_kernel_ptr(false);
+      const void* kern = xp::p2p_tma_kernel_ptr(0);
       if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, xp::p2p_tma_smem())) != cudaSuccess)
         return cuda_failed("cudaFuncSetAttribute", e);
       g_noalloc_dev[dev] = static_cast<unsigned char*>(ptr);
@@ -128,7 +128,7 @@ extern "C" xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t byt
   cfg.attrs = at;
   cfg.numAttrs = 1;
   void* args[] = {&p};
-  if ((e = cudaLaunchKernelExC(&cfg, xp::p2p_tma_kernel_ptr(false), args)) != cudaSuccess)
+  if ((e = cudaLaunchKernelExC(&cfg, xp::p2p_tma_kernel_ptr(0), args)) != cudaSuccess)
     return cuda_failed("cudaLaunchKernelExC", e);
   if (dev_status &&
       (e = cudaMemcpyAsync(dev_status, &status->code, sizeof(int32_t), cudaMemcpyDeviceToDevice, st)) != cudaSuccess)

@@ -107,15 +107,30 @@ struct Entries {
   __device__ __forceinline__ const Stripe& stripe(u64 s) const { return s + 1 == nsteps ? last : full; }
 };
 
-template <bool kZeroCopy>
+// Modes of the kernel.  The posted modes replace head/tail by the
+// receiver-driven credit FIFO ("RDMA and GPUDirect" §4.3; "NCCL transport data
+// transfer (二)", netTransport): the receiver writes post entries {addr, size,
+// idx} into the channel's post FIFO, the sender writes each chunk at the
+// address of the post whose idx is step + 1 and answers with a completion
+// {size, idx}.  Copy mode posts the receiver's staging slots (the receiver
+// then copies them out, as in SIMPLE); direct mode posts dst itself.
+enum : int { kModeSimple = 0, kModeZeroCopy = 1, kModePostedCopy = 2, kModePostedDirect = 3 };
+
+template <int kMode>
 __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams p) {
+  constexpr bool kZeroCopy = kMode == kModeZeroCopy;
+  constexpr bool kPosted = kMode >= kModePostedCopy;
+  constexpr bool kDirect = kMode == kModePostedDirect;
+  constexpr bool kToUser = kZeroCopy || kDirect;   // the sender writes dst itself
   extern __shared__ __align__(128) char stage_mem[];
   __shared__ __align__(8) u64 bars[kMaxSlots];
   __shared__ __align__(8) u64 full[kTmaStages];
   __shared__ __align__(8) u64 empty[kTmaStages];   // receiver: stage free again
   __shared__ u64 s_base;
-  __shared__ u64 s_mirror;   // latest head (sender) or tail (receiver) seen by the watcher
+  __shared__ u64 s_mirror;   // latest head / post (sender) or tail / completion (receiver) seen by the watcher
   __shared__ u64 s_done;     // sender: steps [0, s_done) have their bulk stores complete
+  __shared__ u64 s_addr[kPosted ? kMaxSlots : 1];   // posted sender: address and size of each slot's post
+  __shared__ u64 s_cap[kPosted ? kMaxSlots : 1];
   __shared__ int s_stop;
 
   const int warp = threadIdx.x >> 5;
@@ -123,7 +138,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   const unsigned crank = cluster_ctarank();
   const int ch = blockIdx.x / p.csize;
   const int G = p.lanes;                        // sender lanes
-  const int GR = kZeroCopy ? 1 : p.rlanes;      // receiver lanes
+  const int GR = kToUser ? 1 : p.rlanes;        // receiver lanes
   const bool sender = crank < (unsigned)G;
   const int lane_id = sender ? (int)crank : (int)crank - G;
   const int GS = sender ? G : GR;               // lanes of this CTA's side
@@ -140,12 +155,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   u64* basew = reinterpret_cast<u64*>(ctl + kBaseOff);
   long long* sizew = reinterpret_cast<long long*>(ctl + kSizeOff);
   char* slots = p.slots + (u64)ch * p.ch_stride;
+  char* pctl = kPosted ? p.pctl + (u64)ch * kPostCtlBytes : nullptr;
+  u64* posts = reinterpret_cast<u64*>(pctl + kPostOff);   // entry k: words 8k (addr), 8k+1 (size), 8k+2 (idx)
+  u64* cq = reinterpret_cast<u64*>(pctl + kComplOff);     // entry k: words 2k (size), 2k+1 (idx)
+  if (kPosted) basew = reinterpret_cast<u64*>(pctl + kPostBaseOff);
 
   u64 lo, hi;
   channel_range(p.nbytes, p.nchannels, ch, &lo, &hi);
   const u64 len = hi - lo;
   const u64 nsteps = (len + S - 1) / S;
   const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch};
+  auto step_size = [&](u64 s) -> u64 { return (len - s * S) < S ? (len - s * S) : S; };
 
   if (threadIdx.x == 0) {
     s_base = ld_relaxed(basew);
@@ -175,9 +195,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   const u64 pol_slot = policy_evict_last();     // FIFO slots: reused every N steps
   const u64 pol_user = policy_evict_first();    // src / dst: read or written once
 
+  // receiver side of the posted modes: post chunk s (copy: staging slot
+  // (base + s) % N, whole; direct: its place in dst, its exact size)
+  auto post = [&](u64 s) {
+    const u64 k = (base + s) % N;
+    const u64 addr = kDirect ? reinterpret_cast<u64>(p.dst + lo + s * S) : reinterpret_cast<u64>(slots + k * S);
+    st_relaxed(posts + 8 * k, addr);
+    st_relaxed(posts + 8 * k + 1, kDirect ? step_size(s) : S);
+    st_release(posts + 8 * k + 2, base + s + 1);
+  };
+
   if (run && lane == 0) {
-    if (kZeroCopy && !sender) {
-      if (warp == 1) {
+    if (kToUser && !sender) {
+      if (warp == 1 && kZeroCopy) {
         // zero-copy receiver: post the destination, echo tail into head
         u64 v = 0, tcache = 0;
         if (wait_word(ptrx, 0, v, w, XP_WAIT_PTR_EXCHANGE)) {
@@ -189,6 +219,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           }
           if (j == nsteps) st_relaxed(basew, base + nsteps);
         }
+      } else if (warp == 1 && kDirect) {
+        // direct-posted receiver: keep up to N posts of dst outstanding,
+        // take the completions in order and check the size each reports
+        const u64 first = nsteps < N ? nsteps : N;
+        for (u64 s = 0; s < first; ++s) post(s);
+        atomicMax(&p.status->max_occupancy, (unsigned)first);
+        u64 j = 0;
+        for (; j < nsteps; ++j) {
+          const u64 k = (base + j) % N;
+          u64 c = 0;
+          if (!wait_geq(cq + 2 * k + 1, base + j + 1, c, w, XP_WAIT_COMPLETION)) break;
+          const u64 got = ld_relaxed(cq + 2 * k);
+          if (c != base + j + 1 || got != step_size(j)) {
+            report(w, XP_ERR_BOUNDS, XP_WAIT_COMPLETION, c != base + j + 1 ? c : got,
+                   c != base + j + 1 ? base + j + 1 : step_size(j));
+            break;
+          }
+          if (j + N < nsteps) post(j + N);
+        }
+        if (j == nsteps) st_relaxed(basew, base + nsteps);
       }
     } else if (warp == 0) {
       Entries en;
@@ -199,7 +249,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       bool ok = true;
       if (sender) {
         // ---------------- sender mover ----------------
-        constexpr int kLook = kZeroCopy ? kLookZeroCopy : kLookSend;
+        constexpr int kLook = kToUser ? kLookZeroCopy : kLookSend;
         auto issue_load = [&](u64 q) {
           u64 s, e;
           en.locate(q, &s, &e);
@@ -222,9 +272,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         int since = 0;
         for (u64 s = 0; s < nsteps && ok; ++s) {
           const u64 step = base + s;
-          if (step + 1 > N && hcache < step + 1 - N) {
+          // credit: head (SIMPLE, zero copy) or this step's post (posted modes)
+          const u64 need = kPosted ? step + 1 : (step + 1 > N ? step + 1 - N : 0);
+          if (need && hcache < need) {
             const u64 h = ld_acquire_cta_shared(&s_mirror);
-            if (h >= step + 1 - N) {
+            if (h >= need) {
               hcache = h;
             } else {
               if (pending >= 0) {
@@ -233,18 +285,29 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
                 st_release_cta_shared(&s_done, (u64)pending + 1);
                 pending = -1;
               }
-              if (!wait_mirror(&s_mirror, step + 1 - N, hcache, w, XP_WAIT_HEAD)) { ok = false; break; }
+              if (!wait_mirror(&s_mirror, need, hcache, w, kPosted ? XP_WAIT_POST : XP_WAIT_HEAD)) { ok = false; break; }
             }
           }
           fence_proxy_async_global();
           const u64 off = s * S;
           const Stripe& st = en.stripe(s);
-          char* to = kZeroCopy ? dstp + off : slots + (step % N) * S;
+          char* to;
+          if (kPosted) {
+            const u64 a = s_addr[step % N];
+            if (a % 16 || step_size(s) > s_cap[step % N]) {
+              report(w, XP_ERR_BOUNDS, XP_WAIT_POST, a % 16 ? a : step_size(s), a % 16 ? 16 : s_cap[step % N]);
+              ok = false;
+              break;
+            }
+            to = reinterpret_cast<char*>(a);
+          } else {
+            to = kZeroCopy ? dstp + off : slots + (step % N) * S;
+          }
           for (u64 e = 0; e < st.nent; ++e, ++j) {
             const uint32_t k = (uint32_t)(j % K);
             if (!mbar_wait_cta(smem_addr(&full[k]), (uint32_t)((j / K) & 1), w)) { ok = false; break; }
             const uint32_t nb = entry_bytes(st, e);
-            if (nb) bulk_store(to + st.b0 + e * kTmaChunk, sm0 + k * kTmaChunk, nb, kZeroCopy ? pol_user : pol_slot);
+            if (nb) bulk_store(to + st.b0 + e * kTmaChunk, sm0 + k * kTmaChunk, nb, kToUser ? pol_user : pol_slot);
             bulk_commit();
             if (jl < total) {
               // the stage of entry jl last held entry jl - K, whose store is
@@ -261,7 +324,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           }
           if (!ok) break;
           if (st.rag) copy_bytes(p.src + lo + off + st.b0 + st.fb, to + st.b0 + st.fb, st.rag);
-          if (!kZeroCopy && lane_id == 0) sizew[step % N] = (long long)((len - off) < S ? (len - off) : S);
+          if (kMode == kModeSimple && lane_id == 0) sizew[step % N] = (long long)step_size(s);
           if (pending >= 0) {
             bulk_wait<0>();
             fence_proxy_async_global();
@@ -277,19 +340,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         }
       } else {
         // ---------------- receiver loader ----------------
-        // waits for tail (mirrored), copies the step's ragged bytes, and
-        // loads the stripe's entries from the slot as stages become free
+        // waits for tail or the completion (mirrored), copies the step's
+        // ragged bytes, and loads the stripe's entries from the slot as
+        // stages become free
         u64 tcache = 0;
         for (u64 s = 0; s < nsteps && ok; ++s) {
           const u64 step = base + s;
-          if (!wait_mirror(&s_mirror, step + 1, tcache, w, XP_WAIT_TAIL)) { ok = false; break; }
+          if (!wait_mirror(&s_mirror, step + 1, tcache, w, kPosted ? XP_WAIT_COMPLETION : XP_WAIT_TAIL)) {
+            ok = false;
+            break;
+          }
           fence_proxy_async_global();
           const u64 off = s * S;
-          const u64 sz = (len - off) < S ? (len - off) : S;
           const char* from = slots + (step % N) * S;
-          if (lane_id == 0) {
+          if (!kPosted && lane_id == 0) {
             const long long got = (long long)ld_relaxed(reinterpret_cast<const u64*>(sizew + step % N));
-            if (got != (long long)sz) report(w, XP_ERR_BOUNDS, XP_WAIT_SIZE_WORD, (u64)got, sz);
+            if (got != (long long)step_size(s)) report(w, XP_ERR_BOUNDS, XP_WAIT_SIZE_WORD, (u64)got, step_size(s));
           }
           const Stripe& st = en.stripe(s);
           if (st.rag) copy_bytes(from + st.b0 + st.fb, p.dst + lo + off + st.b0 + st.fb, st.rag);
@@ -344,6 +410,39 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         }
       }
       bulk_wait<0>();
+    } else if (warp == 2 && kPosted) {
+      // ---------------- watcher (posted modes) ----------------
+      // sender: takes the posts in order, keeps each one's address and size
+      // in shared memory and mirrors the count; receiver (copy mode): takes
+      // the completions in order, checks their sizes and mirrors the count
+      WaitClock clk;
+      for (u64 m = 0; m < nsteps; ++m) {
+        const u64 k = (base + m) % N;
+        const u64* idx = sender ? posts + 8 * k + 2 : cq + 2 * k + 1;
+        const u64 want = base + m + 1;
+        u64 v;
+        bool ok = true;
+        while ((v = ld_acquire(idx)) < want) {
+          if (!clk.tick(w, sender ? XP_WAIT_POST : XP_WAIT_COMPLETION, v, want)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (v != want) {   // an entry from the future: the FIFO is corrupt
+          report(w, XP_ERR_BOUNDS, sender ? XP_WAIT_POST : XP_WAIT_COMPLETION, v, want);
+          break;
+        }
+        if (sender) {
+          s_addr[k] = ld_relaxed(posts + 8 * k);
+          s_cap[k] = ld_relaxed(posts + 8 * k + 1);
+        } else {
+          const u64 got = ld_relaxed(cq + 2 * k);
+          if (got != step_size(m)) {
+            report(w, XP_ERR_BOUNDS, XP_WAIT_COMPLETION, got, step_size(m));
+            break;
+          }
+        }
+        st_release_cta_shared(&s_mirror, want);
+        clk = WaitClock();   // the timeout counts time without progress
+      }
     } else if (warp == 2) {
       // ---------------- watcher ----------------
       // sender: head, as far as the last step's credit needs it;
@@ -364,12 +463,27 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       }
     } else if (warp == 3 && leader_cta) {
       // ---------------- publisher ----------------
+      // SIMPLE / zero copy: tail (sender) or head (receiver) = step + 1;
+      // posted: the completion of the step (sender) or the post N steps on
+      // (receiver, copy mode)
       u64 s = 0;
       unsigned max_occ = 0;
+      if (kPosted && !sender) {
+        const u64 first = nsteps < N ? nsteps : N;
+        for (u64 q = 0; q < first; ++q) post(q);
+        max_occ = (unsigned)first;
+      }
       for (; s < nsteps; ++s) {
         const u64 step = base + s;
         if (!mbar_wait(smem_addr(&bars[step % N]), (uint32_t)((s / N) & 1), w, XP_WAIT_SLOT_BARRIER, step)) break;
-        if (sender) {
+        if (kPosted) {
+          if (sender) {
+            st_relaxed(cq + 2 * (step % N), step_size(s));
+            st_release(cq + 2 * (step % N) + 1, step + 1);
+          } else if (s + N < nsteps) {
+            post(s + N);
+          }
+        } else if (sender) {
           st_release(tail, step + 1);
           const u64 h = ld_relaxed(head);
           const u64 occ = step + 1 - h;
@@ -382,8 +496,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           st_release(head, step + 1);
         }
       }
+      if (sender != kPosted) atomicMax(&p.status->max_occupancy, max_occ);
       if (sender) {
-        atomicMax(&p.status->max_occupancy, max_occ);
         if (kZeroCopy && s == nsteps) {
           u64 hc = 0;
           if (wait_geq(head, base + nsteps, hc, w, XP_WAIT_HEAD)) st_release(ptrx, 0);
@@ -397,11 +511,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   cluster_sync_all();
 }
 
-template __global__ void p2p_tma_kernel<false>(const P2pParams);
-template __global__ void p2p_tma_kernel<true>(const P2pParams);
+template __global__ void p2p_tma_kernel<kModeSimple>(const P2pParams);
+template __global__ void p2p_tma_kernel<kModeZeroCopy>(const P2pParams);
+template __global__ void p2p_tma_kernel<kModePostedCopy>(const P2pParams);
+template __global__ void p2p_tma_kernel<kModePostedDirect>(const P2pParams);
 
-void* p2p_tma_kernel_ptr(bool zero_copy) {
-  return zero_copy ? reinterpret_cast<void*>(&p2p_tma_kernel<true>) : reinterpret_cast<void*>(&p2p_tma_kernel<false>);
+void* p2p_tma_kernel_ptr(int mode) {
+  switch (mode) {
+    case kModeZeroCopy: return reinterpret_cast<void*>(&p2p_tma_kernel<kModeZeroCopy>);
+    case kModePostedCopy: return reinterpret_cast<void*>(&p2p_tma_kernel<kModePostedCopy>);
+    case kModePostedDirect: return reinterpret_cast<void*>(&p2p_tma_kernel<kModePostedDirect>);
+    default: return reinterpret_cast<void*>(&p2p_tma_kernel<kModeSimple>);
+  }
 }
 int p2p_tma_threads() { return kTmaThreads; }
 int p2p_tma_smem() { return kTmaSmem; }

@@ -19,7 +19,7 @@ XP_PROTO_SIMPLE, XP_PROTO_LL = 0, 1
 XP_PLACE_DEVICE, XP_PLACE_HOST_MAPPED = 0, 1
 XP_U8, XP_U32, XP_I32, XP_F32, XP_BF16 = range(5)
 (XP_WAIT_NONE, XP_WAIT_HEAD, XP_WAIT_TAIL, XP_WAIT_PTR_EXCHANGE, XP_WAIT_LL_FLAG, XP_WAIT_SLOT_BARRIER,
- XP_WAIT_SIZE_WORD, XP_WAIT_OCCUPANCY, XP_WAIT_STICKY) = range(9)
+ XP_WAIT_SIZE_WORD, XP_WAIT_OCCUPANCY, XP_WAIT_STICKY, XP_WAIT_POST, XP_WAIT_COMPLETION) = range(11)
 
 # every entry point include/xp.h declares
 EXPORTS = [
@@ -27,7 +27,7 @@ EXPORTS = [
     "xp_send_recv_zero_copy", "xp_fifo_status", "xp_fifo_reset", "xp_ll_pingpong", "xp_ring_create",
     "xp_ring_destroy", "xp_ring_set_lanes", "xp_ring_allreduce_virtual", "xp_ring_status", "xp_ring_reset",
     "xp_set_spin_timeout_ns", "xp_abort", "xp_status_string", "xp_last_error", "xp_version",
-    "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes",
+    "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes", "xp_send_recv_posted",
 ]
 
 
@@ -40,7 +40,7 @@ class xp_report(ctypes.Structure):
 class xp_channel_desc(ctypes.Structure):
     _fields_ = [("ctl", ctypes.c_void_p), ("slots", ctypes.c_void_p), ("slot_stride", ctypes.c_size_t),
                 ("nslots", ctypes.c_int), ("proto", ctypes.c_int), ("placement", ctypes.c_int),
-                ("lanes", ctypes.c_int), ("recv_lanes", ctypes.c_int)]
+                ("lanes", ctypes.c_int), ("recv_lanes", ctypes.c_int), ("posted", ctypes.c_void_p)]
 
 
 class XpError(RuntimeError):
@@ -62,6 +62,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         "xp_fifo_describe": [P, I, ctypes.POINTER(xp_channel_desc)],
         "xp_send_recv": [P, P, P, Z, P],
         "xp_send_recv_zero_copy": [P, P, P, Z, P],
+        "xp_send_recv_posted": [P, P, P, Z, I, P],
         "xp_fifo_status": [P, I, ctypes.POINTER(xp_report)],
         "xp_fifo_reset": [P],
         "xp_ll_pingpong": [P, P, I, ctypes.POINTER(U64), P],
@@ -155,6 +156,11 @@ def xp_send_recv(fifo: int, src, dst, nbytes: int, stream=None) -> None:
 def xp_send_recv_zero_copy(fifo: int, src, dst, nbytes: int, stream=None) -> None:
     _check(_lib.xp_send_recv_zero_copy(fifo, _ptr(src), _ptr(dst), nbytes, _stream(stream)),
            "xp_send_recv_zero_copy")
+
+
+def xp_send_recv_posted(fifo: int, src, dst, nbytes: int, direct: bool = False, stream=None) -> None:
+    _check(_lib.xp_send_recv_posted(fifo, _ptr(src), _ptr(dst), nbytes, 1 if direct else 0, _stream(stream)),
+           "xp_send_recv_posted")
 
 
 def xp_fifo_status(fifo: int, sync: bool = True) -> tuple[int, xp_report]:

@@ -33,7 +33,11 @@
  *   - Operations on one FIFO (or one ring) must be ordered: issue them on one
  *     stream, or synchronise between them.  Step counters live on the device
  *     and carry over from one operation to the next, so captured CUDA graphs
- *     may be replayed.
+ *     may be replayed.  A call made while its stream is being captured
+ *     records no completion event: synchronise the stream a graph replays on
+ *     before xp_fifo_status / xp_ring_status, and make the first call on a
+ *     FIFO or ring outside any capture (it sets kernel attributes and
+ *     queries occupancy).
  *   - Argument errors return immediately (no launch).  A CUDA error from a
  *     launch returns XP_ERR_CUDA (message in xp_last_error()).  Errors found
  *     on the device (a wait that timed out, a size word or occupancy out of
@@ -80,7 +84,7 @@ typedef enum { XP_U8 = 0, XP_U32 = 1, XP_I32 = 2, XP_F32 = 3, XP_BF16 = 4 } xp_d
 typedef enum {
   XP_WAIT_NONE = 0, XP_WAIT_HEAD = 1, XP_WAIT_TAIL = 2, XP_WAIT_PTR_EXCHANGE = 3,
   XP_WAIT_LL_FLAG = 4, XP_WAIT_SLOT_BARRIER = 5, XP_WAIT_SIZE_WORD = 6, XP_WAIT_OCCUPANCY = 7,
-  XP_WAIT_STICKY = 8
+  XP_WAIT_STICKY = 8, XP_WAIT_POST = 9, XP_WAIT_COMPLETION = 10
 } xp_wait_site;
 
 typedef struct xp_fifo xp_fifo;   /* opaque, owned by the library */
@@ -104,7 +108,11 @@ typedef struct {
  * at +128, uint64 ptrExchange at +256, uint64 step base at +384 and int64
  * size words (one per slot, -1 = never written) at +512; slots points at
  * slot 0, slot k at slots + k * slot_stride.  LL slots hold 16-byte lines
- * {data0, flag0, data1, flag1} (uint32 each). */
+ * {data0, flag0, data1, flag1} (uint32 each).  posted points at the
+ * channel's receiver-driven credit FIFO (xp_send_recv_posted): 64 post
+ * entries of 64 bytes {uint64 addr, uint64 size, uint64 idx, pad} at +0, 64
+ * completion entries of 16 bytes {uint64 size, uint64 idx} at +4096 and the
+ * uint64 step base of the next posted operation at +5120. */
 typedef struct {
   void* ctl;
   void* slots;
@@ -114,6 +122,7 @@ typedef struct {
   int placement;
   int lanes;          /* sender CTAs per channel   */
   int recv_lanes;     /* receiver CTAs per channel */
+  void* posted;
 } xp_channel_desc;
 
 /* Create a FIFO of `nchannels` independent channels, each with `nslots`
@@ -170,6 +179,30 @@ xp_status xp_send_recv(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_
  * slots are not touched.  SIMPLE FIFOs only; any byte count. */
 xp_status xp_send_recv_zero_copy(xp_fifo* f, const void* src, void* dst, size_t bytes,
                                  xp_stream_t stream);
+
+/* Transfer with receiver-driven credit ([rdma] §4.3: the receiver tells the
+ * sender where to write through a FIFO of {addr, size, idx} entries;
+ * [transfer] netTransport copy and zero-copy modes).  Per channel (split as
+ * in xp_send_recv) the receiver keeps up to nslots posts outstanding: post j
+ * of an operation carries idx = base + j + 1, where base counts the channel's
+ * chunks of all earlier posted operations, and names where chunk j (at most
+ * slot_bytes bytes) may land.  The sender waits for the post whose idx is
+ * base + j + 1 in FIFO entry (base + j) % nslots, checks that the chunk fits
+ * its size and that its address is 16-byte aligned (else XP_ERR_BOUNDS,
+ * where = XP_WAIT_POST), writes the chunk there and then the completion
+ * {size, idx} into completion entry (base + j) % nslots; the receiver takes
+ * the completions in order, checks each size (else XP_ERR_BOUNDS, where =
+ * XP_WAIT_COMPLETION) and posts chunk j + nslots once chunk j is consumed.
+ *   direct == 0 (copy mode): posts name the FIFO's staging slots, whole; the
+ *     receiver copies each landed slot to dst, then re-posts it.  Uses the
+ *     FIFO's lanes and receiver lanes.
+ *   direct != 0: posts name dst itself, exactly the chunk; the slots are not
+ *     touched.  One receiver CTA per channel.
+ * Head, tail, size words and ptrExchange are not used, so posted and other
+ * operations may alternate on one FIFO.  SIMPLE FIFOs in device memory only
+ * (XP_ERR_INVALID otherwise); any byte count; src and dst must not overlap. */
+xp_status xp_send_recv_posted(xp_fifo* f, const void* src, void* dst, size_t bytes, int direct,
+                              xp_stream_t stream);
 
 /* Outcome of the FIFO's last operation.  sync != 0 first waits for the
  * FIFO's last stream; sync == 0 reads whatever the device has written so far

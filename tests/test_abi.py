@@ -26,7 +26,7 @@ def xp():
 
 def test_every_declared_symbol_is_exported(xp):
     names = _declared()
-    assert len(names) == 22, names
+    assert len(names) == 23, names
     out = subprocess.run(["nm", "-D", "--defined-only", xp.library_path()], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (xp_[a-z0-9_]+)", out))
     assert set(names) <= exported
@@ -61,6 +61,7 @@ def test_null_handles_are_rejected(xp):
     for fn in (xp._lib.xp_fifo_set_lanes, xp._lib.xp_ring_set_lanes):
         assert fn(None, 1) == xp.XP_ERR_INVALID
     assert xp._lib.xp_send_recv(None, None, None, 16, None) == xp.XP_ERR_INVALID
+    assert xp._lib.xp_send_recv_posted(None, None, None, 16, 0, None) == xp.XP_ERR_INVALID
     assert xp._lib.xp_fifo_destroy(None) == xp.XP_OK
     assert xp._lib.xp_ring_destroy(None) == xp.XP_OK
     with pytest.raises(xp.XpError):
