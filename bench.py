@@ -221,6 +221,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--mib", type=int, default=0,
                     help="profiling only: move the first MiB of the workload instead of 1 GiB")
+    ap.add_argument("--rows", default="",
+                    help="profiling only: run just these comma-separated row groups (" + ",".join(ROW_GROUPS) +
+                         ") after the step, without the end-to-end and CPU legs")
+    ap.add_argument("--ring-mib", type=int, default=0,
+                    help="profiling only: MiB per rank of the ring row instead of 256")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
@@ -300,7 +305,9 @@ def main():
 
     if args.mib:
         out["config"]["workload"] += f" (profiling case: first {args.mib} MiB)"
-    if rank == 0 and not args.no_rows:
+    if rank == 0 and args.rows:
+        out["rows"] = rows(torch, xp, hbm_peak, set(args.rows.split(",")), args.ring_mib)
+    elif rank == 0 and not args.no_rows:
         out["e2e"] = e2e_row(torch, xp, fifo, src_np, stream)
         out["rows"] = rows(torch, xp, hbm_peak)
         rate, desc = cpu_oracle_rate(args.cpu_budget)
@@ -340,179 +347,199 @@ def e2e_row(torch, xp, fifo, src_np, stream, iters=5):
             "ms_per_step": ms}
 
 
-def rows(torch, xp, hbm_peak):
+ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "loopback", "ll", "host_fifo", "ring")
+
+
+def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
     s = torch.cuda.Stream()
     res = {}
+
+    def want(name):
+        return only is None or name in only
+
     # HBM copy ceiling, re-measured in this run (read + write bytes)
-    a = torch.empty(GIB // 2, dtype=torch.bfloat16, device="cuda")
-    b = torch.empty_like(a)
-    with torch.cuda.stream(s):
-        t = time_events(torch, s, lambda: b.copy_(a), 10)
-    res["hbm_copy_gbs_this_run"] = 2 * GIB / (min(t) * 1e-3) / 1e9
-    del a, b
+    if want("hbm"):
+        a = torch.empty(GIB // 2, dtype=torch.bfloat16, device="cuda")
+        b = torch.empty_like(a)
+        with torch.cuda.stream(s):
+            t = time_events(torch, s, lambda: b.copy_(a), 10)
+        res["hbm_copy_gbs_this_run"] = 2 * GIB / (min(t) * 1e-3) / 1e9
+        del a, b
 
-    # zero copy, 1 GiB through the same geometry
     w = workloads.SIMPLE_MULTI
-    src = torch.from_numpy(workloads.normal_bf16_bits(w["nelems"], w["seed"])).to("cuda")
-    dst = torch.empty_like(src)
-    n = src.numel() * 2
-    zc = {}
-    for lanes in (4, 8):
+    if want("zero_copy") or want("simple_lanes1") or want("posted"):
+        src = torch.from_numpy(workloads.normal_bf16_bits(w["nelems"], w["seed"])).to("cuda")
+        dst = torch.empty_like(src)
+        n = src.numel() * 2
+
+    if want("zero_copy"):
+        # zero copy, 1 GiB through the same geometry
+        zc = {}
+        for lanes in (4, 8):
+            f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
+            xp.xp_fifo_set_lanes(f, lanes)
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    xp.xp_send_recv_zero_copy(f, src, dst, n, s)
+                t = time_events(torch, s, lambda: xp.xp_send_recv_zero_copy(f, src, dst, n, s), 50)
+            st, _ = xp.xp_fifo_status(f, True)
+            ok = st == xp.XP_OK and torch.equal(dst, src)
+            ms = statistics.median(t)
+            zc[f"lanes{lanes}"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "frac_of_hbm": 2 * n / (ms * 1e-3) / 1e9 / hbm_peak,
+                                   "exact": bool(ok)}
+            xp.xp_fifo_destroy(f)
+        res["zero_copy"] = zc
+
+    if want("simple_lanes1"):
+        # SIMPLE with one sender CTA and one receiver CTA per channel (lanes 1)
         f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
-        xp.xp_fifo_set_lanes(f, lanes)
-        with torch.cuda.stream(s):
-            for _ in range(5):
-                xp.xp_send_recv_zero_copy(f, src, dst, n, s)
-            t = time_events(torch, s, lambda: xp.xp_send_recv_zero_copy(f, src, dst, n, s), 50)
-        st, _ = xp.xp_fifo_status(f, True)
-        ok = st == xp.XP_OK and torch.equal(dst, src)
-        ms = statistics.median(t)
-        zc[f"lanes{lanes}"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "frac_of_hbm": 2 * n / (ms * 1e-3) / 1e9 / hbm_peak,
-                               "exact": bool(ok)}
-        xp.xp_fifo_destroy(f)
-    res["zero_copy"] = zc
-
-    # SIMPLE with one sender CTA and one receiver CTA per channel (lanes 1)
-    f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
-    with torch.cuda.stream(s):
-        for _ in range(3):
-            xp.xp_send_recv(f, src, dst, n, s)
-        t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 20)
-    ms = statistics.median(t)
-    res["simple_lanes1"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "frac_of_hbm": 4 * n / (ms * 1e-3) / 1e9 / hbm_peak}
-    xp.xp_fifo_destroy(f)
-
-    # receiver-driven credit (posts {addr, size, idx}): copy mode through the
-    # staging slots (4 bytes of HBM traffic per payload byte) and direct
-    # mode into dst (2 bytes per payload byte)
-    posted = {}
-    for direct, lanes, rl in ((False, 6, 7), (True, 8, None)):
-        f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
-        xp.xp_fifo_set_lanes(f, lanes)
-        if rl:
-            xp.xp_fifo_set_recv_lanes(f, rl)
-        dst.zero_()
-        with torch.cuda.stream(s):
-            for _ in range(5):
-                xp.xp_send_recv_posted(f, src, dst, n, direct, s)
-            t = time_events(torch, s, lambda: xp.xp_send_recv_posted(f, src, dst, n, direct, s), 50)
-        st, _ = xp.xp_fifo_status(f, True)
-        ms = statistics.median(t)
-        per = 2 if direct else 4
-        posted["direct" if direct else "copy"] = {
-            "lanes": lanes, "recv_lanes": rl or 1, "gbs": n / (ms * 1e-3) / 1e9, "ms": ms,
-            "frac_of_hbm": per * n / (ms * 1e-3) / 1e9 / hbm_peak, "exact": bool(st == xp.XP_OK and torch.equal(dst, src))}
-        xp.xp_fifo_destroy(f)
-    res["posted"] = posted
-    del src, dst
-
-    # SIMPLE loopback: 1 MiB, one sender CTA -> one receiver CTA, 8 x 64 KiB
-    wl = workloads.SIMPLE_LOOPBACK
-    src = torch.from_numpy(workloads.uniform_bytes(wl["nbytes"], wl["seed"])).to("cuda")
-    dst = torch.empty_like(src)
-    f = xp.xp_fifo_create(1, wl["nslots"], wl["slot_bytes"])
-    with torch.cuda.stream(s):
-        for _ in range(10):
-            xp.xp_send_recv(f, src, dst, wl["nbytes"], s)
-        t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, wl["nbytes"], s), 200)
-    ms = statistics.median(t)
-    res["simple_loopback_1MiB"] = {"us": ms * 1e3, "gbs": wl["nbytes"] / (ms * 1e-3) / 1e9}
-    xp.xp_fifo_destroy(f)
-
-    # LL: size sweep through one FIFO, and the device-side ping-pong
-    wl = workloads.LL_SWEEP
-    f = xp.xp_fifo_create(1, wl["nslots"], wl["slot_bytes"], xp.XP_PROTO_LL)
-    sweep = {}
-    for size in wl["sizes"]:
-        words = torch.from_numpy(workloads.uniform_u32(size // 4, wl["seed"])).to("cuda")
-        out_t = torch.empty_like(words)
-        with torch.cuda.stream(s):
-            for _ in range(10):
-                xp.xp_send_recv(f, words, out_t, size, s)
-            t = time_events(torch, s, lambda: xp.xp_send_recv(f, words, out_t, size, s), 100)
-        sweep[str(size)] = statistics.median(t) * 1e3
-    st, _ = xp.xp_fifo_status(f, True)
-    ab = xp.xp_fifo_create(1, wl["nslots"], wl["slot_bytes"], xp.XP_PROTO_LL)
-    ns = xp.xp_ll_pingpong(f, ab, 20000, s)
-    xp.xp_fifo_destroy(ab)
-    xp.xp_fifo_destroy(f)
-    sizes = np.array(wl["sizes"], float)
-    us = np.array([sweep[str(x)] for x in wl["sizes"]])
-    beta, alpha = np.polyfit(sizes, us, 1)          # us = alpha + beta * bytes
-    res["ll"] = {"us_per_message_with_launch": sweep, "pingpong_one_way_us": ns / 2 / 20000 / 1e3,
-                 "alpha_us": float(alpha), "beta_gbs": float(1e-3 / beta) if beta > 0 else None, "status": st}
-
-    # host-placed FIFO: 256 MiB fp32, 8 channels x 8 x 1 MiB in pinned host memory
-    wh = workloads.HOST_FIFO
-    src = torch.from_numpy(workloads.uniform_f32(wh["nelems"], wh["seed"])).to("cuda")
-    dst = torch.empty_like(src)
-    n = src.numel() * 4
-    host = {}
-    for lanes in (1, 2, 4):
-        f = xp.xp_fifo_create(wh["nchannels"], wh["nslots"], wh["slot_bytes"], xp.XP_PROTO_SIMPLE,
-                              xp.XP_PLACE_HOST_MAPPED)
-        xp.xp_fifo_set_lanes(f, lanes)
         with torch.cuda.stream(s):
             for _ in range(3):
                 xp.xp_send_recv(f, src, dst, n, s)
-            t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 10)
-        st, _ = xp.xp_fifo_status(f, True)
+            t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 20)
         ms = statistics.median(t)
-        host[f"lanes{lanes}"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "exact": bool(st == 0 and torch.equal(dst, src))}
+        res["simple_lanes1"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "frac_of_hbm": 4 * n / (ms * 1e-3) / 1e9 / hbm_peak}
         xp.xp_fifo_destroy(f)
-    # ceiling: concurrent pinned cudaMemcpyAsync D2H || H2D of the same size
-    hp = torch.empty(n, dtype=torch.uint8).pin_memory()
-    hq = torch.empty(n, dtype=torch.uint8).pin_memory()
-    d1 = torch.empty(n, dtype=torch.uint8, device="cuda")
-    d2 = torch.empty(n, dtype=torch.uint8, device="cuda")
-    s2 = torch.cuda.Stream()
-    best = 1e30
-    for i in range(6):
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s)
-        s2.wait_event(e0)
-        with torch.cuda.stream(s):
-            d1.copy_(hp, non_blocking=True)
-        with torch.cuda.stream(s2):
-            hq.copy_(d2, non_blocking=True)
-        s.wait_stream(s2)
-        e1.record(s)
-        torch.cuda.synchronize()
-        if i >= 1:
-            best = min(best, e0.elapsed_time(e1))
-    ceiling = n / (best * 1e-3) / 1e9
-    top = max(v["gbs"] for v in host.values())
-    res["host_fifo"] = {"by_lanes": host, "ceiling_concurrent_memcpy_gbs": ceiling, "frac_of_ceiling": top / ceiling}
-    del src, dst, hp, hq, d1, d2
 
-    # virtual ring allreduce: 8 ranks x 256 MiB fp32, 8 channels x 8 x 512 KiB
-    wr = workloads.RING
-    xs = [torch.from_numpy(x).to("cuda") for x in workloads.ring_inputs(wr["nranks"], wr["nelems"], "f32", wr["seed_base"])]
-    ys = [torch.empty_like(x) for x in xs]
-    ring = {}
-    for lanes in (1,):
-        r = xp.xp_ring_create(wr["nranks"], wr["nchannels"], wr["nslots"], wr["slot_bytes"])
-        try:
-            xp.xp_ring_set_lanes(r, lanes)
+    if want("posted"):
+        # receiver-driven credit (posts {addr, size, idx}): copy mode through the
+        # staging slots (4 bytes of HBM traffic per payload byte) and direct
+        # mode into dst (2 bytes per payload byte)
+        posted = {}
+        for direct, lanes, rl in ((False, 6, 7), (True, 8, None)):
+            f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
+            xp.xp_fifo_set_lanes(f, lanes)
+            if rl:
+                xp.xp_fifo_set_recv_lanes(f, rl)
+            dst.zero_()
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    xp.xp_send_recv_posted(f, src, dst, n, direct, s)
+                t = time_events(torch, s, lambda: xp.xp_send_recv_posted(f, src, dst, n, direct, s), 50)
+            st, _ = xp.xp_fifo_status(f, True)
+            ms = statistics.median(t)
+            per = 2 if direct else 4
+            posted["direct" if direct else "copy"] = {
+                "lanes": lanes, "recv_lanes": rl or 1, "gbs": n / (ms * 1e-3) / 1e9, "ms": ms,
+                "frac_of_hbm": per * n / (ms * 1e-3) / 1e9 / hbm_peak, "exact": bool(st == xp.XP_OK and torch.equal(dst, src))}
+            xp.xp_fifo_destroy(f)
+        res["posted"] = posted
+    if want("zero_copy") or want("simple_lanes1") or want("posted"):
+        del src, dst
+
+    if want("loopback"):
+        # SIMPLE loopback: 1 MiB, one sender CTA -> one receiver CTA, 8 x 64 KiB
+        wl = workloads.SIMPLE_LOOPBACK
+        src = torch.from_numpy(workloads.uniform_bytes(wl["nbytes"], wl["seed"])).to("cuda")
+        dst = torch.empty_like(src)
+        f = xp.xp_fifo_create(1, wl["nslots"], wl["slot_bytes"])
+        with torch.cuda.stream(s):
+            for _ in range(10):
+                xp.xp_send_recv(f, src, dst, wl["nbytes"], s)
+            t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, wl["nbytes"], s), 200)
+        ms = statistics.median(t)
+        res["simple_loopback_1MiB"] = {"us": ms * 1e3, "gbs": wl["nbytes"] / (ms * 1e-3) / 1e9}
+        xp.xp_fifo_destroy(f)
+
+    if want("ll"):
+        # LL: size sweep through one FIFO, and the device-side ping-pong
+        wl = workloads.LL_SWEEP
+        f = xp.xp_fifo_create(1, wl["nslots"], wl["slot_bytes"], xp.XP_PROTO_LL)
+        sweep = {}
+        for size in wl["sizes"]:
+            words = torch.from_numpy(workloads.uniform_u32(size // 4, wl["seed"])).to("cuda")
+            out_t = torch.empty_like(words)
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    xp.xp_send_recv(f, words, out_t, size, s)
+                t = time_events(torch, s, lambda: xp.xp_send_recv(f, words, out_t, size, s), 100)
+            sweep[str(size)] = statistics.median(t) * 1e3
+        st, _ = xp.xp_fifo_status(f, True)
+        ab = xp.xp_fifo_create(1, wl["nslots"], wl["slot_bytes"], xp.XP_PROTO_LL)
+        ns = xp.xp_ll_pingpong(f, ab, 20000, s)
+        xp.xp_fifo_destroy(ab)
+        xp.xp_fifo_destroy(f)
+        sizes = np.array(wl["sizes"], float)
+        us = np.array([sweep[str(x)] for x in wl["sizes"]])
+        beta, alpha = np.polyfit(sizes, us, 1)          # us = alpha + beta * bytes
+        res["ll"] = {"us_per_message_with_launch": sweep, "pingpong_one_way_us": ns / 2 / 20000 / 1e3,
+                     "alpha_us": float(alpha), "beta_gbs": float(1e-3 / beta) if beta > 0 else None, "status": st}
+
+    if want("host_fifo"):
+        # host-placed FIFO: 256 MiB fp32, 8 channels x 8 x 1 MiB in pinned host memory
+        wh = workloads.HOST_FIFO
+        src = torch.from_numpy(workloads.uniform_f32(wh["nelems"], wh["seed"])).to("cuda")
+        dst = torch.empty_like(src)
+        n = src.numel() * 4
+        host = {}
+        for lanes in (1, 2, 4):
+            f = xp.xp_fifo_create(wh["nchannels"], wh["nslots"], wh["slot_bytes"], xp.XP_PROTO_SIMPLE,
+                                  xp.XP_PLACE_HOST_MAPPED)
+            xp.xp_fifo_set_lanes(f, lanes)
             with torch.cuda.stream(s):
                 for _ in range(3):
-                    xp.xp_ring_allreduce_virtual(r, xs, ys, wr["nelems"], xp.XP_F32, s)
-                t = time_events(torch, s, lambda: xp.xp_ring_allreduce_virtual(r, xs, ys, wr["nelems"], xp.XP_F32, s), 10)
-        except xp.XpError as e:
-            ring[f"lanes{lanes}"] = {"error": str(e)}
+                    xp.xp_send_recv(f, src, dst, n, s)
+                t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 10)
+            st, _ = xp.xp_fifo_status(f, True)
+            ms = statistics.median(t)
+            host[f"lanes{lanes}"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "exact": bool(st == 0 and torch.equal(dst, src))}
+            xp.xp_fifo_destroy(f)
+        # ceiling: concurrent pinned cudaMemcpyAsync D2H || H2D of the same size
+        hp = torch.empty(n, dtype=torch.uint8).pin_memory()
+        hq = torch.empty(n, dtype=torch.uint8).pin_memory()
+        d1 = torch.empty(n, dtype=torch.uint8, device="cuda")
+        d2 = torch.empty(n, dtype=torch.uint8, device="cuda")
+        s2 = torch.cuda.Stream()
+        best = 1e30
+        for i in range(6):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            s2.wait_event(e0)
+            with torch.cuda.stream(s):
+                d1.copy_(hp, non_blocking=True)
+            with torch.cuda.stream(s2):
+                hq.copy_(d2, non_blocking=True)
+            s.wait_stream(s2)
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 1:
+                best = min(best, e0.elapsed_time(e1))
+        ceiling = n / (best * 1e-3) / 1e9
+        top = max(v["gbs"] for v in host.values())
+        res["host_fifo"] = {"by_lanes": host, "ceiling_concurrent_memcpy_gbs": ceiling, "frac_of_ceiling": top / ceiling}
+        del src, dst, hp, hq, d1, d2
+
+    if want("ring"):
+        # virtual ring allreduce: 8 ranks x 256 MiB fp32, 8 channels x 8 x 512 KiB
+        wr = workloads.RING
+        nel = (ring_mib << 18) if ring_mib else wr["nelems"]
+        xs = [torch.from_numpy(x).to("cuda") for x in workloads.ring_inputs(wr["nranks"], nel, "f32", wr["seed_base"])]
+        ys = [torch.empty_like(x) for x in xs]
+        ring = {}
+        for lanes in (1,):
+            r = xp.xp_ring_create(wr["nranks"], wr["nchannels"], wr["nslots"], wr["slot_bytes"])
+            try:
+                xp.xp_ring_set_lanes(r, lanes)
+                with torch.cuda.stream(s):
+                    for _ in range(3):
+                        xp.xp_ring_allreduce_virtual(r, xs, ys, nel, xp.XP_F32, s)
+                    t = time_events(torch, s, lambda: xp.xp_ring_allreduce_virtual(r, xs, ys, nel, xp.XP_F32, s), 10)
+            except xp.XpError as e:
+                ring[f"lanes{lanes}"] = {"error": str(e)}
+                xp.xp_ring_destroy(r)
+                continue
+            st, _ = xp.xp_ring_status(r, True)
+            ms = statistics.median(t)
+            n = nel * 4
+            P = wr["nranks"]
+            alg = (6 * P - 4) * n
+            ring[f"lanes{lanes}"] = {"ms": ms, "algbw_gbs": n / (ms * 1e-3) / 1e9,
+                                     "hbm_gbs": alg / (ms * 1e-3) / 1e9, "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak,
+                                     "status": st}
             xp.xp_ring_destroy(r)
-            continue
-        st, _ = xp.xp_ring_status(r, True)
-        ms = statistics.median(t)
-        n = wr["nelems"] * 4
-        P = wr["nranks"]
-        alg = (6 * P - 4) * n
-        ring[f"lanes{lanes}"] = {"ms": ms, "algbw_gbs": n / (ms * 1e-3) / 1e9,
-                                 "hbm_gbs": alg / (ms * 1e-3) / 1e9, "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak,
-                                 "status": st}
-        xp.xp_ring_destroy(r)
-    res["ring_f32"] = ring
+        res["ring_f32"] = ring
+
     return res
 
 
