@@ -11,7 +11,8 @@ reference leg may import or run anything in this package.  The library itself
 never routes through it: there is no CPU fallback.
 
 Entry points:
-* `simple_transfer`, `ll_transfer`, `zero_copy_transfer`, `posted_transfer`:
+* `simple_transfer`, `ll_transfer`, `zero_copy_transfer`, `posted_transfer`,
+  `ce_transfer`:
   move a buffer through C channels under a seeded random interleaving and
   return the result;
 * `ring_allreduce`: the ring as state machines; `ring_order_sum`: the plain
@@ -25,13 +26,14 @@ arithmetic rounded to fp32, against int64 sums for int32, against the
 fp64 sum within the standard error bound, and the pages' printed sizes and
 ring-neighbour example (tests/golden/).
 """
-from .fifo import (Deadlock, LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender,
+from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, Deadlock, LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender,
                    ProtocolViolation, SimpleFifo, SimpleReceiver, SimpleSender, System, ZeroCopyChannel,
                    ZeroCopyReceiver, ZeroCopySender, explore, ll_flag, run)
 from .partition import (channel_byte_ranges, ring_channel_ranges, ring_chunk_elems, ring_next,
                         ring_prev, ring_rounds, ring_schedule, slot_steps)
 from .ring import ring_order_sum, ring_system
-from .transfer import (ll_transfer, posted_transfer, ring_allreduce, simple_transfer, zero_copy_transfer)
+from .transfer import (ce_transfer, ll_transfer, posted_transfer, ring_allreduce, simple_transfer,
+                       zero_copy_transfer)
 
 __all__ = [
     "Deadlock", "ProtocolViolation", "SimpleFifo", "SimpleSender", "SimpleReceiver", "LLFifo",
@@ -40,4 +42,5 @@ __all__ = [
     "ring_channel_ranges", "ring_chunk_elems", "ring_rounds", "ring_schedule", "ring_order_sum",
     "ring_system", "simple_transfer", "ll_transfer", "zero_copy_transfer", "ring_allreduce",
     "PostedChannel", "PostedSender", "PostedReceiver", "posted_transfer",
+    "CEFifo", "CESender", "CEProxy", "CEReceiver", "ce_transfer",
 ]

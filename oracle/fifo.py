@@ -757,6 +757,191 @@ class PostedSender(Actor):
 
 
 # --------------------------------------------------------------------------
+# Copy-engine (proxy) mode ("NCCL transport data transfer (二)", p2pTransport
+# cudaMemcopy mode (CE mode) and shmTransport useMemcpy mode)
+# --------------------------------------------------------------------------
+
+class CopyRing:
+    """N slots of S bytes with the ownership checks of SimpleFifo: a slot is
+    written only after its previous step was read out, and read only while it
+    holds the step asked for."""
+
+    def __init__(self, nslots: int, slot_bytes: int):
+        self.N, self.S = nslots, slot_bytes
+        self.slots = np.zeros((nslots, slot_bytes), np.uint8)
+        self.owner = [None] * nslots
+        self.consumed = [True] * nslots
+
+    def put(self, step: int, data: np.ndarray, what: str):
+        k = step % self.N
+        if not self.consumed[k]:
+            raise ProtocolViolation(f"{what}: step {step} overwrites slot {k} holding unread step {self.owner[k]}")
+        self.slots[k, :len(data)] = data
+        self.owner[k] = step
+        self.consumed[k] = False
+
+    def take(self, step: int, nbytes: int, what: str) -> np.ndarray:
+        k = step % self.N
+        if self.owner[k] != step or self.consumed[k]:
+            raise ProtocolViolation(f"{what}: step {step} reads slot {k} holding step {self.owner[k]} "
+                                    f"(read={self.consumed[k]})")
+        self.consumed[k] = True
+        return self.slots[k, :nbytes].copy()
+
+    def state(self):
+        return (self.slots.tobytes(), tuple(self.owner), tuple(self.consumed))
+
+
+class CEFifo:
+    """One channel of the proxy mode: the sender kernel fills ring 0 (its own
+    send buffer) and publishes tails[0]; proxy hop h copies each step from
+    ring h to ring h + 1 (one cudaMemcpy per step) and publishes tails[h + 1]
+    once the copy has completed; the receiver kernel drains the last ring and
+    returns head, the one credit counter of the chain.  hops = 1 is the p2p
+    CE mode (send buffer -> receive buffer); hops = 2 is the shm useMemcpy
+    mode (send buffer -> host shared buffer -> receive buffer).  The sender
+    writes each step's size word before tails[0]; the hops copy that many
+    bytes and the receiver checks it."""
+
+    def __init__(self, nslots: int, slot_bytes: int, hops: int = 1, step0: int = 0):
+        if nslots < 1 or slot_bytes < 1 or hops < 1:
+            raise ValueError("need nslots, slot_bytes, hops >= 1")
+        self.N, self.S, self.H = nslots, slot_bytes, hops
+        self.rings = [CopyRing(nslots, slot_bytes) for _ in range(hops + 1)]
+        self.tails = [step0] * (hops + 1)
+        self.head = step0
+        self.size = [-1] * nslots
+        self.max_occupancy = 0
+
+    def check(self):
+        chain = self.tails + [self.head]
+        for a, b in zip(chain, chain[1:]):
+            if b > a:
+                raise ProtocolViolation(f"counter chain out of order: {chain}")
+        occ = self.tails[0] - self.head
+        if occ > self.N:
+            raise ProtocolViolation(f"tail {self.tails[0]} exceeds head {self.head} + N {self.N}")
+        self.max_occupancy = max(self.max_occupancy, occ)
+
+    def state(self):
+        return (tuple(self.tails), self.head, tuple(self.size), tuple(r.state() for r in self.rings))
+
+
+class _Stepper(Actor):
+    """Walks steps base .. base + nsteps - 1 through a fixed order of phases."""
+    DONE = -1
+
+    def _start(self, base, nsteps, order):
+        self.base, self.nsteps, self.order = base, nsteps, order
+        self.step = base
+        self.phase = order[0] if nsteps else self.DONE
+
+    def done(self):
+        return self.phase == self.DONE
+
+    def _advance(self):
+        i = self.order.index(self.phase)
+        if i + 1 < len(self.order):
+            self.phase = self.order[i + 1]
+        else:
+            self.step += 1
+            self.phase = self.order[0] if self.step < self.base + self.nsteps else self.DONE
+
+    def state(self):
+        return (self.step, self.phase)
+
+
+class CESender(_Stepper):
+    """Per step: wait credit (step < head + N), fill send-ring slot and size
+    word, publish tails[0].  `fault`: "skip_credit"."""
+    WAIT, FILL, PUB = range(3)
+
+    def __init__(self, fifo: CEFifo, src: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.f, self.src, self.lo, self.hi, self.fault = fifo, src, lo, hi, fault
+        self._start(fifo.tails[0], ceil_div(hi - lo, fifo.S), (self.WAIT, self.FILL, self.PUB))
+        self.name = f"ce-send[{lo}:{hi}]"
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT:
+            return [0] if self.fault == "skip_credit" or self.step < self.f.head + self.f.N else []
+        return [0]
+
+    def fire(self, choice):
+        if self.phase == self.FILL:
+            off = self.lo + (self.step - self.base) * self.f.S
+            piece = self.src[off:min(self.hi, off + self.f.S)]
+            self.f.rings[0].put(self.step, piece, "sender")
+            self.f.size[self.step % self.f.N] = len(piece)
+        elif self.phase == self.PUB:
+            self.f.tails[0] = self.step + 1
+        self._advance()
+
+
+class CEProxy(_Stepper):
+    """Hop h of the host proxy.  Per step: wait tails[h] > step, copy the
+    step's size-word bytes from ring h to ring h + 1, and publish
+    tails[h + 1] = step + 1 once that copy is complete.
+    `fault`: "tail_before_copy" (publishes before the copy lands)."""
+    WAIT, COPY, PUB = range(3)
+
+    def __init__(self, fifo: CEFifo, hop: int, nsteps: int, fault: str | None = None):
+        self.f, self.h, self.fault = fifo, hop, fault
+        order = (self.WAIT, self.PUB, self.COPY) if fault == "tail_before_copy" else (self.WAIT, self.COPY, self.PUB)
+        self._start(fifo.tails[hop + 1], nsteps, order)
+        self.name = f"ce-proxy[{hop}]"
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT:
+            return [0] if self.f.tails[self.h] > self.step else []
+        return [0]
+
+    def fire(self, choice):
+        if self.phase == self.COPY:
+            n = self.f.size[self.step % self.f.N]
+            if not 1 <= n <= self.f.S:
+                raise ProtocolViolation(f"proxy hop {self.h}: size word {n} of step {self.step}")
+            data = self.f.rings[self.h].take(self.step, n, f"proxy hop {self.h}")
+            self.f.rings[self.h + 1].put(self.step, data, f"proxy hop {self.h}")
+        elif self.phase == self.PUB:
+            self.f.tails[self.h + 1] = self.step + 1
+        self._advance()
+
+
+class CEReceiver(_Stepper):
+    """Per step: wait tails[H] > step, check the size word, copy the receive
+    ring's slot to dst, publish head.  `fault`: "head_before_copy"."""
+    WAIT, COPY, PUB = range(3)
+
+    def __init__(self, fifo: CEFifo, dst: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.f, self.dst, self.lo, self.hi, self.fault = fifo, dst, lo, hi, fault
+        order = (self.WAIT, self.PUB, self.COPY) if fault == "head_before_copy" else (self.WAIT, self.COPY, self.PUB)
+        self._start(fifo.head, ceil_div(hi - lo, fifo.S), order)
+        self.name = f"ce-recv[{lo}:{hi}]"
+
+    def choices(self):
+        if self.phase == self.DONE:
+            return []
+        if self.phase == self.WAIT:
+            return [0] if self.f.tails[-1] > self.step else []
+        return [0]
+
+    def fire(self, choice):
+        if self.phase == self.COPY:
+            off = self.lo + (self.step - self.base) * self.f.S
+            n = min(self.hi, off + self.f.S) - off
+            if self.f.size[self.step % self.f.N] != n:
+                raise ProtocolViolation(f"size word {self.f.size[self.step % self.f.N]} != {n}")
+            self.dst[off:off + n] = self.f.rings[-1].take(self.step, n, "receiver")
+        elif self.phase == self.PUB:
+            self.f.head = self.step + 1
+        self._advance()
+
+
+# --------------------------------------------------------------------------
 # Schedulers
 # --------------------------------------------------------------------------
 

@@ -10,8 +10,9 @@ from __future__ import annotations
 
 import numpy as np
 
-from .fifo import (LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender, SimpleFifo,
-                   SimpleReceiver, SimpleSender, System, ZeroCopyChannel, ZeroCopyReceiver, ZeroCopySender, run)
+from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, LLFifo, LLReceiver, LLSender, PostedChannel,
+                   PostedReceiver, PostedSender, SimpleFifo, SimpleReceiver, SimpleSender, System, ZeroCopyChannel,
+                   ZeroCopyReceiver, ZeroCopySender, run)
 from .partition import channel_byte_ranges
 from .ring import ring_system
 
@@ -77,6 +78,23 @@ def posted_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: in
             actors += [PostedSender(c, src, lo, hi), PostedReceiver(c, dst, lo, hi, direct=direct)]
     ev = run(System(actors, chans, [dst]), seed=seed)
     return dst, chans, ev
+
+
+def ce_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: int, hops: int = 1, seed: int = 0,
+                fifos: list[CEFifo] | None = None):
+    """Proxy-mode transfer of the byte buffer `src` through `hops` host-driven
+    copies per slot-step; returns (dst, fifos, events)."""
+    src = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
+    dst = np.zeros_like(src)
+    if fifos is None:
+        fifos = [CEFifo(nslots, slot_bytes, hops) for _ in range(nchannels)]
+    actors = []
+    for f, (lo, hi) in zip(fifos, channel_byte_ranges(len(src), nchannels)):
+        if hi > lo:
+            n = -(-(hi - lo) // f.S)
+            actors += [CESender(f, src, lo, hi)] + [CEProxy(f, h, n) for h in range(f.H)] + [CEReceiver(f, dst, lo, hi)]
+    ev = run(System(actors, fifos, [dst]), seed=seed)
+    return dst, fifos, ev
 
 
 def ring_allreduce(inputs: list[np.ndarray], nchannels: int, nslots: int, slot_bytes: int, seed: int = 0):
