@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "xp_internal.h"
+#include "xp_proxy.h"
 
 namespace xp {
 void* p2p_kernel_ptr(bool zero_copy);
@@ -253,6 +254,13 @@ struct xp_fifo {
   size_t ctl_region = 0;
   size_t pctl_region = 0;
   size_t ch_stride = 0;
+  // proxy (copy-engine) mode, set up by xp_fifo_enable_ce
+  Mem ce_mem;              // mapped host memory: per-channel proxy blocks
+  Mem ring_mem;            // device: send ring (+ receive ring for 2 hops)
+  char* send_ring = nullptr;
+  char* recv_ring = nullptr;
+  int hops = 0;
+  xp::Pump* pump = nullptr;
 };
 
 struct xp_ring {
@@ -339,9 +347,60 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
 xp_status xp_fifo_destroy(xp_fifo* f) {
   if (!f) return XP_OK;
   cudaDeviceSynchronize();
+  xp::pump_stop(f->pump);
   common_free(f->cm);
   mem_free(f->mem);
+  mem_free(f->ce_mem);
+  mem_free(f->ring_mem);
   delete f;
+  return XP_OK;
+}
+
+static xp::PumpConfig pump_config(const xp_fifo* f) {
+  xp::PumpConfig cfg;
+  cfg.device = f->cm.device;
+  cfg.nchannels = f->C;
+  cfg.nslots = f->N;
+  cfg.slot_bytes = f->S;
+  cfg.ch_stride = f->ch_stride;
+  cfg.hops = f->hops;
+  cfg.ce_host = f->ce_mem.host;
+  cfg.rings[0] = f->send_ring;
+  if (f->hops == 1) {
+    cfg.rings[1] = f->slots;
+  } else {
+    cfg.rings[1] = f->mem.host + (f->slots - f->mem.dev);   // the FIFO's own slots, host view
+    cfg.rings[2] = f->recv_ring;
+  }
+  return cfg;
+}
+
+xp_status xp_fifo_enable_ce(xp_fifo* f) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "the proxy mode needs a SIMPLE FIFO");
+  if (f->pump) return XP_OK;
+  xp_status s = check_device(f->cm);
+  if (s != XP_OK) return s;
+  const int hops = f->place == XP_PLACE_DEVICE ? 1 : 2;
+  const size_t ring = (size_t)f->C * f->ch_stride;
+  if ((s = mem_alloc(f->ring_mem, hops * ring, XP_PLACE_DEVICE)) != XP_OK) return s;
+  if ((s = mem_alloc(f->ce_mem, (size_t)f->C * xp::kCeCtlBytes, XP_PLACE_HOST_MAPPED)) != XP_OK) {
+    mem_free(f->ring_mem);
+    return s;
+  }
+  memset(f->ce_mem.host, 0, f->ce_mem.bytes);
+  f->hops = hops;
+  f->send_ring = f->ring_mem.dev;
+  f->recv_ring = hops == 1 ? f->slots : f->ring_mem.dev + ring;
+  std::string err;
+  f->pump = xp::pump_start(pump_config(f), &err);
+  if (!f->pump) {
+    mem_free(f->ce_mem);
+    mem_free(f->ring_mem);
+    f->hops = 0;
+    f->send_ring = f->recv_ring = nullptr;
+    return fail(XP_ERR_CUDA, "%s", err.c_str());
+  }
   return XP_OK;
 }
 
@@ -375,10 +434,13 @@ xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out) 
   out->lanes = f->lanes;
   out->recv_lanes = f->rlanes;
   out->posted = f->pctl + (size_t)channel * xp::kPostCtlBytes;
+  out->ce = f->pump ? f->ce_mem.dev + (size_t)channel * xp::kCeCtlBytes : nullptr;
+  out->send_ring = f->pump ? f->send_ring + (size_t)channel * f->ch_stride : nullptr;
+  out->recv_ring = f->pump ? f->recv_ring + (size_t)channel * f->ch_stride : nullptr;
   return XP_OK;
 }
 
-enum { kOpSimple = 0, kOpZeroCopy = 1, kOpPostedCopy = 2, kOpPostedDirect = 3 };   // p2p_tma_kernel_ptr modes
+enum { kOpSimple = 0, kOpZeroCopy = 1, kOpPostedCopy = 2, kOpPostedDirect = 3, kOpProxy = 4 };   // p2p_tma_kernel_ptr modes
 
 static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream, int mode) {
   const bool zero_copy = mode == kOpZeroCopy;
@@ -392,6 +454,7 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   if (zero_copy && f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "zero copy needs a SIMPLE FIFO");
   if (posted && (f->proto != XP_PROTO_SIMPLE || f->place != XP_PLACE_DEVICE))
     return fail(XP_ERR_INVALID, "posted transfers need a SIMPLE FIFO in device memory");
+  if (mode == kOpProxy && !f->pump) return fail(XP_ERR_INVALID, "the proxy mode is not enabled (xp_fifo_enable_ce)");
   if (f->proto == XP_PROTO_LL && bytes % 8) return fail(XP_ERR_INVALID, "LL moves whole 8-byte lines: bytes %% 8 != 0");
   xp_status s = check_device(f->cm);
   if (s != XP_OK) return s;
@@ -399,6 +462,10 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   xp::P2pParams p = {};
   p.ctl = f->ctl;
   p.pctl = f->pctl;
+  p.ce = f->ce_mem.dev;
+  p.send_ring = f->send_ring;
+  p.recv_ring = f->recv_ring;
+  p.hops = f->hops;
   p.slots = f->slots;
   p.ch_stride = f->ch_stride;
   p.src = static_cast<const char*>(src);
@@ -421,8 +488,8 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     p.lanes = f->lanes;
     p.rlanes = (zero_copy || mode == kOpPostedDirect) ? 1 : f->rlanes;
     csize = p.lanes + p.rlanes;
-    if (f->place == XP_PLACE_DEVICE) {
-      // HBM FIFO: bulk copies through shared memory
+    if (f->place == XP_PLACE_DEVICE || mode == kOpProxy) {
+      // HBM FIFO (or the proxy mode's device rings): bulk copies through shared memory
       kernel = xp::p2p_tma_kernel_ptr(mode);
       block = xp::p2p_tma_threads();
       smem = xp::p2p_tma_smem();
@@ -435,6 +502,7 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   p.csize = csize;
   XP_CUDA(cudaMemsetAsync(f->cm.status, 0, xp::kStatusClearBytes, st));
   if ((s = launch(kernel, f->C * csize, block, csize, &p, st, smem)) != XP_OK) return s;
+  if (mode == kOpProxy) xp::pump_kick(f->pump);
   return record_done(f->cm, st);
 }
 
@@ -450,15 +518,30 @@ xp_status xp_send_recv_posted(xp_fifo* f, const void* src, void* dst, size_t byt
   return p2p_op(f, src, dst, bytes, stream, direct ? kOpPostedDirect : kOpPostedCopy);
 }
 
+xp_status xp_send_recv_ce(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream) {
+  return p2p_op(f, src, dst, bytes, stream, kOpProxy);
+}
+
 xp_status xp_fifo_status(xp_fifo* f, int sync, xp_report* report) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
-  return read_status(f->cm, sync, report);
+  const xp_status s = read_status(f->cm, sync, report);
+  if (const char* e = xp::pump_error(f->pump)) xp::set_last_error(e);
+  return s;
 }
 
 xp_status xp_fifo_reset(xp_fifo* f) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (f->cm.used) XP_CUDA(cudaEventSynchronize(f->cm.done));
   XP_CUDA(cudaMemset(f->cm.status, 0, sizeof(DevStatus)));
+  if (f->pump) {
+    // restart the pump on zeroed proxy counters
+    xp::pump_stop(f->pump);
+    f->pump = nullptr;
+    memset(f->ce_mem.host, 0, f->ce_mem.bytes);
+    std::string err;
+    f->pump = xp::pump_start(pump_config(f), &err);
+    if (!f->pump) return fail(XP_ERR_CUDA, "%s", err.c_str());
+  }
   return mem_init(f->mem, f->C);
 }
 

@@ -33,6 +33,18 @@ constexpr int kPostOff = 0;
 constexpr int kComplOff = 64 * kMaxSlots;
 constexpr int kPostBaseOff = kComplOff + 16 * kMaxSlots;
 
+// Per-channel block of the proxy (copy-engine) mode, in mapped host memory:
+// tail[h] for h = 0 .. 2 on their own lines (tail[0] written by the sender
+// kernel, tail[h + 1] by the host pump once hop h's copy of a step has
+// completed), head (written by the receiver kernel), the step base of the
+// next proxy operation, and the sender's int64 size word per slot.
+constexpr int kCeCtlBytes = 2048;
+constexpr int kCeMaxHops = 2;
+constexpr int kCeTailOff = 0;          // tail[h] at kCeTailOff + 128 h
+constexpr int kCeHeadOff = 384;
+constexpr int kCeBaseOff = 512;
+constexpr int kCeSizeOff = 640;        // kMaxSlots int64 size words
+
 constexpr int kCopyWarps = 16;                  // data-moving warps per CTA
 constexpr int kP2pThreads = 32 * (kCopyWarps + 1);   // + 1 publisher warp
 constexpr int kRingThreads = 32 * (kCopyWarps + 2);  // + tail and head publishers
@@ -59,6 +71,10 @@ constexpr int kStatusClearBytes = 64;
 struct P2pParams {
   char* ctl;                      // nchannels control blocks
   char* pctl;                     // nchannels posted-FIFO blocks (posted transfers)
+  char* ce;                       // nchannels proxy-mode blocks (mapped host memory)
+  char* send_ring;                // proxy mode: the sender's own slots, same geometry as `slots`
+  char* recv_ring;                // proxy mode: the slots the receiver drains
+  int hops;                       // proxy mode: host-driven copies per slot-step (1 or 2)
   char* slots;                    // channel c's slot k at slots + c*ch_stride + k*slot_bytes
   unsigned long long ch_stride;
   const char* src;

@@ -114,7 +114,28 @@ struct Entries {
 // address of the post whose idx is step + 1 and answers with a completion
 // {size, idx}.  Copy mode posts the receiver's staging slots (the receiver
 // then copies them out, as in SIMPLE); direct mode posts dst itself.
-enum : int { kModeSimple = 0, kModeZeroCopy = 1, kModePostedCopy = 2, kModePostedDirect = 3 };
+//
+// Proxy mode ("NCCL transport data transfer (二)", p2pTransport CE mode and
+// shmTransport useMemcpy mode): the sender fills its own send ring and
+// publishes tail[0]; a host thread copies each slot-step with the copy engines
+// through `hops` rings and publishes tail[hops]; the receiver drains the last
+// ring.  Counters, size words and the step base then live in mapped host
+// memory and are accessed at .sys scope.
+enum : int { kModeSimple = 0, kModeZeroCopy = 1, kModePostedCopy = 2, kModePostedDirect = 3, kModeProxy = 4 };
+
+// control-word access at the scope the mode needs
+template <bool kSys>
+__device__ __forceinline__ u64 ctl_acquire(const u64* p) { return kSys ? ld_acquire_sys(p) : ld_acquire(p); }
+template <bool kSys>
+__device__ __forceinline__ u64 ctl_relaxed(const u64* p) { return kSys ? ld_relaxed_sys(p) : ld_relaxed(p); }
+template <bool kSys>
+__device__ __forceinline__ void ctl_release(u64* p, u64 v) {
+  if (kSys) st_release_sys(p, v); else st_release(p, v);
+}
+template <bool kSys>
+__device__ __forceinline__ void ctl_store(u64* p, u64 v) {
+  if (kSys) st_relaxed_sys(p, v); else st_relaxed(p, v);
+}
 
 template <int kMode>
 __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams p) {
@@ -122,6 +143,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   constexpr bool kPosted = kMode >= kModePostedCopy;
   constexpr bool kDirect = kMode == kModePostedDirect;
   constexpr bool kToUser = kZeroCopy || kDirect;   // the sender writes dst itself
+  constexpr bool kProxy = kMode == kModeProxy;
   extern __shared__ __align__(128) char stage_mem[];
   __shared__ __align__(8) u64 bars[kMaxSlots];
   __shared__ __align__(8) u64 full[kTmaStages];
@@ -159,6 +181,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   u64* posts = reinterpret_cast<u64*>(pctl + kPostOff);   // entry k: words 8k (addr), 8k+1 (size), 8k+2 (idx)
   u64* cq = reinterpret_cast<u64*>(pctl + kComplOff);     // entry k: words 2k (size), 2k+1 (idx)
   if (kPosted) basew = reinterpret_cast<u64*>(pctl + kPostBaseOff);
+  u64* tail_pub = tail;         // the tail this kernel's sender publishes
+  char* slots_send = slots;     // where the sender writes, and where the receiver reads
+  char* slots_recv = slots;
+  if (kProxy) {
+    char* ce = p.ce + (u64)ch * kCeCtlBytes;
+    tail_pub = reinterpret_cast<u64*>(ce + kCeTailOff);
+    tail = reinterpret_cast<u64*>(ce + kCeTailOff + 128 * p.hops);
+    head = reinterpret_cast<u64*>(ce + kCeHeadOff);
+    basew = reinterpret_cast<u64*>(ce + kCeBaseOff);
+    sizew = reinterpret_cast<long long*>(ce + kCeSizeOff);
+    slots_send = p.send_ring + (u64)ch * p.ch_stride;
+    slots_recv = p.recv_ring + (u64)ch * p.ch_stride;
+  }
 
   u64 lo, hi;
   channel_range(p.nbytes, p.nchannels, ch, &lo, &hi);
@@ -168,7 +203,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   auto step_size = [&](u64 s) -> u64 { return (len - s * S) < S ? (len - s * S) : S; };
 
   if (threadIdx.x == 0) {
-    s_base = ld_relaxed(basew);
+    s_base = ctl_relaxed<kProxy>(basew);
     s_stop = 0;
     if (*reinterpret_cast<volatile int*>(&p.status->sticky)) {
       s_stop = 1;
@@ -301,7 +336,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
             }
             to = reinterpret_cast<char*>(a);
           } else {
-            to = kZeroCopy ? dstp + off : slots + (step % N) * S;
+            to = kZeroCopy ? dstp + off : slots_send + (step % N) * S;
           }
           for (u64 e = 0; e < st.nent; ++e, ++j) {
             const uint32_t k = (uint32_t)(j % K);
@@ -324,7 +359,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           }
           if (!ok) break;
           if (st.rag) copy_bytes(p.src + lo + off + st.b0 + st.fb, to + st.b0 + st.fb, st.rag);
-          if (kMode == kModeSimple && lane_id == 0) sizew[step % N] = (long long)step_size(s);
+          if ((kMode == kModeSimple || kProxy) && lane_id == 0)
+            ctl_store<kProxy>(reinterpret_cast<u64*>(sizew + step % N), step_size(s));
           if (pending >= 0) {
             bulk_wait<0>();
             fence_proxy_async_global();
@@ -352,9 +388,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           }
           fence_proxy_async_global();
           const u64 off = s * S;
-          const char* from = slots + (step % N) * S;
+          const char* from = slots_recv + (step % N) * S;
           if (!kPosted && lane_id == 0) {
-            const long long got = (long long)ld_relaxed(reinterpret_cast<const u64*>(sizew + step % N));
+            const long long got = (long long)ctl_relaxed<kProxy>(reinterpret_cast<const u64*>(sizew + step % N));
             if (got != (long long)step_size(s)) report(w, XP_ERR_BOUNDS, XP_WAIT_SIZE_WORD, (u64)got, step_size(s));
           }
           const Stripe& st = en.stripe(s);
@@ -452,7 +488,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       u64 seen = 0;
       WaitClock clk;
       while (seen < target) {
-        const u64 v = ld_acquire(word);
+        const u64 v = ctl_acquire<kProxy>(word);
         if (v > seen) {
           seen = v;
           st_release_cta_shared(&s_mirror, v);
@@ -484,8 +520,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
             post(s + N);
           }
         } else if (sender) {
-          st_release(tail, step + 1);
-          const u64 h = ld_relaxed(head);
+          ctl_release<kProxy>(tail_pub, step + 1);
+          const u64 h = ctl_relaxed<kProxy>(head);
           const u64 occ = step + 1 - h;
           if (h > step + 1 || occ > N) {
             report(w, XP_ERR_BOUNDS, XP_WAIT_OCCUPANCY, occ, N);
@@ -493,7 +529,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           }
           if (occ > max_occ) max_occ = (unsigned)occ;
         } else {
-          st_release(head, step + 1);
+          ctl_release<kProxy>(head, step + 1);
         }
       }
       if (sender != kPosted) atomicMax(&p.status->max_occupancy, max_occ);
@@ -503,7 +539,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           if (wait_geq(head, base + nsteps, hc, w, XP_WAIT_HEAD)) st_release(ptrx, 0);
         }
       } else if (s == nsteps) {
-        st_relaxed(basew, base + nsteps);
+        ctl_store<kProxy>(basew, base + nsteps);
       }
     }
   }
@@ -515,12 +551,14 @@ template __global__ void p2p_tma_kernel<kModeSimple>(const P2pParams);
 template __global__ void p2p_tma_kernel<kModeZeroCopy>(const P2pParams);
 template __global__ void p2p_tma_kernel<kModePostedCopy>(const P2pParams);
 template __global__ void p2p_tma_kernel<kModePostedDirect>(const P2pParams);
+template __global__ void p2p_tma_kernel<kModeProxy>(const P2pParams);
 
 void* p2p_tma_kernel_ptr(int mode) {
   switch (mode) {
     case kModeZeroCopy: return reinterpret_cast<void*>(&p2p_tma_kernel<kModeZeroCopy>);
     case kModePostedCopy: return reinterpret_cast<void*>(&p2p_tma_kernel<kModePostedCopy>);
     case kModePostedDirect: return reinterpret_cast<void*>(&p2p_tma_kernel<kModePostedDirect>);
+    case kModeProxy: return reinterpret_cast<void*>(&p2p_tma_kernel<kModeProxy>);
     default: return reinterpret_cast<void*>(&p2p_tma_kernel<kModeSimple>);
   }
 }

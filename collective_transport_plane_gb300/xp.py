@@ -27,7 +27,8 @@ EXPORTS = [
     "xp_send_recv_zero_copy", "xp_fifo_status", "xp_fifo_reset", "xp_ll_pingpong", "xp_ring_create",
     "xp_ring_destroy", "xp_ring_set_lanes", "xp_ring_allreduce_virtual", "xp_ring_status", "xp_ring_reset",
     "xp_set_spin_timeout_ns", "xp_abort", "xp_status_string", "xp_last_error", "xp_version",
-    "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes", "xp_send_recv_posted",
+    "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes", "xp_send_recv_posted", "xp_fifo_enable_ce",
+    "xp_send_recv_ce",
 ]
 
 
@@ -40,7 +41,8 @@ class xp_report(ctypes.Structure):
 class xp_channel_desc(ctypes.Structure):
     _fields_ = [("ctl", ctypes.c_void_p), ("slots", ctypes.c_void_p), ("slot_stride", ctypes.c_size_t),
                 ("nslots", ctypes.c_int), ("proto", ctypes.c_int), ("placement", ctypes.c_int),
-                ("lanes", ctypes.c_int), ("recv_lanes", ctypes.c_int), ("posted", ctypes.c_void_p)]
+                ("lanes", ctypes.c_int), ("recv_lanes", ctypes.c_int), ("posted", ctypes.c_void_p),
+                ("ce", ctypes.c_void_p), ("send_ring", ctypes.c_void_p), ("recv_ring", ctypes.c_void_p)]
 
 
 class XpError(RuntimeError):
@@ -63,6 +65,8 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         "xp_send_recv": [P, P, P, Z, P],
         "xp_send_recv_zero_copy": [P, P, P, Z, P],
         "xp_send_recv_posted": [P, P, P, Z, I, P],
+        "xp_fifo_enable_ce": [P],
+        "xp_send_recv_ce": [P, P, P, Z, P],
         "xp_fifo_status": [P, I, ctypes.POINTER(xp_report)],
         "xp_fifo_reset": [P],
         "xp_ll_pingpong": [P, P, I, ctypes.POINTER(U64), P],
@@ -156,6 +160,14 @@ def xp_send_recv(fifo: int, src, dst, nbytes: int, stream=None) -> None:
 def xp_send_recv_zero_copy(fifo: int, src, dst, nbytes: int, stream=None) -> None:
     _check(_lib.xp_send_recv_zero_copy(fifo, _ptr(src), _ptr(dst), nbytes, _stream(stream)),
            "xp_send_recv_zero_copy")
+
+
+def xp_fifo_enable_ce(fifo: int) -> None:
+    _check(_lib.xp_fifo_enable_ce(fifo), "xp_fifo_enable_ce")
+
+
+def xp_send_recv_ce(fifo: int, src, dst, nbytes: int, stream=None) -> None:
+    _check(_lib.xp_send_recv_ce(fifo, _ptr(src), _ptr(dst), nbytes, _stream(stream)), "xp_send_recv_ce")
 
 
 def xp_send_recv_posted(fifo: int, src, dst, nbytes: int, direct: bool = False, stream=None) -> None:

@@ -44,8 +44,9 @@
  *     bounds, an abort request) are reported by xp_fifo_status /
  *     xp_ring_status; after one, the object refuses further work (its next
  *     operations report XP_ERR_ABORTED) until xp_fifo_reset / xp_ring_reset.
- *   - No call allocates memory except *_create; no call spins on the host
- *     except the *_status calls with sync != 0 and *_destroy.
+ *   - No call allocates memory except *_create and xp_fifo_enable_ce; no call
+ *     spins on the host except the *_status calls with sync != 0 and
+ *     *_destroy (the proxy mode's own host thread aside).
  */
 #ifndef XP_H
 #define XP_H
@@ -112,7 +113,10 @@ typedef struct {
  * channel's receiver-driven credit FIFO (xp_send_recv_posted): 64 post
  * entries of 64 bytes {uint64 addr, uint64 size, uint64 idx, pad} at +0, 64
  * completion entries of 16 bytes {uint64 size, uint64 idx} at +4096 and the
- * uint64 step base of the next posted operation at +5120. */
+ * uint64 step base of the next posted operation at +5120.  After
+ * xp_fifo_enable_ce, ce points at the channel's proxy-mode block (mapped host
+ * memory, device view) and send_ring / recv_ring at the channel's slot 0 of
+ * the send ring and of the ring the receiver drains (NULL before). */
 typedef struct {
   void* ctl;
   void* slots;
@@ -123,6 +127,9 @@ typedef struct {
   int lanes;          /* sender CTAs per channel   */
   int recv_lanes;     /* receiver CTAs per channel */
   void* posted;
+  void* ce;
+  void* send_ring;
+  void* recv_ring;
 } xp_channel_desc;
 
 /* Create a FIFO of `nchannels` independent channels, each with `nslots`
@@ -203,6 +210,35 @@ xp_status xp_send_recv_zero_copy(xp_fifo* f, const void* src, void* dst, size_t 
  * (XP_ERR_INVALID otherwise); any byte count; src and dst must not overlap. */
 xp_status xp_send_recv_posted(xp_fifo* f, const void* src, void* dst, size_t bytes, int direct,
                               xp_stream_t stream);
+
+/* Set up the proxy (copy-engine) mode on a SIMPLE FIFO ([transfer]
+ * p2pTransport cudaMemcopy mode and shmTransport useMemcpy mode): allocates
+ * the sender's own send ring in device memory (same geometry as the FIFO's
+ * slots), for a host-placed FIFO also a receive ring in device memory, and
+ * per channel a 2 KiB block in mapped host memory (uint64 tail[h] at +128 h
+ * for h = 0..2, uint64 head at +384, uint64 step base at +512, int64 size
+ * words at +640), and starts a host thread (the pump) that serves every
+ * later xp_send_recv_ce on this FIFO until xp_fifo_destroy.  Device FIFO:
+ * one hop per slot-step, send ring -> the FIFO's slots.  Host-placed FIFO:
+ * two hops, send ring -> the FIFO's slots in host memory -> receive ring.
+ * Calling it again is a no-op.  Errors: XP_ERR_INVALID (not SIMPLE),
+ * XP_ERR_CUDA (allocation or thread setup failed). */
+xp_status xp_fifo_enable_ce(xp_fifo* f);
+
+/* Transfer through the proxy mode (after xp_fifo_enable_ce).  Channels and
+ * slot-steps as in xp_send_recv.  The sender CTAs fill send-ring slot
+ * step % nslots, write its size word and publish tail[0] = step + 1 at
+ * system scope, under the credit step < head + nslots; for each hop h the
+ * pump copies the step's size-word bytes from ring h to ring h + 1 with
+ * cudaMemcpyAsync on its own stream and publishes tail[h + 1] = step + 1 once
+ * that copy has completed; the receiver CTAs wait for the last tail, check
+ * the size word, copy the slot out to dst and publish head.  A size word
+ * outside [1, slot_bytes] stops the pump (the transfer then times out and
+ * xp_fifo_status leaves the pump's message in xp_last_error()).  The pump
+ * keeps serving while the FIFO exists, so captured graphs replay.  Proxy
+ * operations keep their own counters; other operations may alternate with
+ * them on the FIFO. */
+xp_status xp_send_recv_ce(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream);
 
 /* Outcome of the FIFO's last operation.  sync != 0 first waits for the
  * FIFO's last stream; sync == 0 reads whatever the device has written so far

@@ -32,12 +32,14 @@ def _capture(torch, fn):
     return g
 
 
-@pytest.mark.parametrize("mode", ["simple", "zero_copy", "posted_copy", "posted_direct"])
+@pytest.mark.parametrize("mode", ["simple", "zero_copy", "posted_copy", "posted_direct", "ce"])
 def test_p2p_graph_replay(env, mode):
     torch, xp = env
     nchan, nslots, slot, n = 4, 4, 8192, 300007
     fifo = xp.xp_fifo_create(nchan, nslots, slot)
     xp.xp_fifo_set_lanes(fifo, 2)
+    if mode == "ce":
+        xp.xp_fifo_enable_ce(fifo)       # the pump keeps serving replays
     src = torch.zeros(n, dtype=torch.uint8, device="cuda")
     dst = torch.zeros_like(src)
 
@@ -46,6 +48,8 @@ def test_p2p_graph_replay(env, mode):
             xp.xp_send_recv(fifo, src, dst, n, s)
         elif mode == "zero_copy":
             xp.xp_send_recv_zero_copy(fifo, src, dst, n, s)
+        elif mode == "ce":
+            xp.xp_send_recv_ce(fifo, src, dst, n, s)
         else:
             xp.xp_send_recv_posted(fifo, src, dst, n, mode == "posted_direct", s)
 
@@ -56,6 +60,8 @@ def test_p2p_graph_replay(env, mode):
             want = oracle.simple_transfer(src_np, nchan, nslots, slot, seed=i)[0]
         elif mode == "zero_copy":
             want = oracle.zero_copy_transfer(src_np, nchan, nslots, slot, seed=i)[0]
+        elif mode == "ce":
+            want = oracle.ce_transfer(src_np, nchan, nslots, slot, seed=i)[0]
         else:
             want = oracle.posted_transfer(src_np, nchan, nslots, slot, seed=i, direct=mode == "posted_direct")[0]
         src.copy_(torch.from_numpy(src_np))
