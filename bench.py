@@ -347,7 +347,7 @@ def e2e_row(torch, xp, fifo, src_np, stream, iters=5):
             "ms_per_step": ms}
 
 
-ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "loopback", "ll", "host_fifo", "ring")
+ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "ce", "loopback", "ll", "host_fifo", "ring")
 
 
 def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
@@ -367,7 +367,7 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         del a, b
 
     w = workloads.SIMPLE_MULTI
-    if want("zero_copy") or want("simple_lanes1") or want("posted"):
+    if want("zero_copy") or want("simple_lanes1") or want("posted") or want("ce"):
         src = torch.from_numpy(workloads.normal_bf16_bits(w["nelems"], w["seed"])).to("cuda")
         dst = torch.empty_like(src)
         n = src.numel() * 2
@@ -424,7 +424,34 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
                 "frac_of_hbm": per * n / (ms * 1e-3) / 1e9 / hbm_peak, "exact": bool(st == xp.XP_OK and torch.equal(dst, src))}
             xp.xp_fifo_destroy(f)
         res["posted"] = posted
-    if want("zero_copy") or want("simple_lanes1") or want("posted"):
+    if want("ce"):
+        # proxy (copy-engine) mode, one hop: sender CTAs -> send ring, the
+        # library's host pump copies every slot-step with cudaMemcpyAsync,
+        # receiver CTAs drain the FIFO's slots.  Ceiling: one plain
+        # cudaMemcpyAsync of the whole buffer, device to device.
+        ce = {}
+        for lanes in (2, 4):
+            f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
+            xp.xp_fifo_set_lanes(f, lanes)
+            xp.xp_fifo_enable_ce(f)
+            dst.zero_()
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    xp.xp_send_recv_ce(f, src, dst, n, s)
+                t = time_events(torch, s, lambda: xp.xp_send_recv_ce(f, src, dst, n, s), 10)
+            st, _ = xp.xp_fifo_status(f, True)
+            ms = statistics.median(t)
+            ce[f"lanes{lanes}"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms,
+                                   "exact": bool(st == xp.XP_OK and torch.equal(dst, src))}
+            xp.xp_fifo_destroy(f)
+        with torch.cuda.stream(s):
+            t = time_events(torch, s, lambda: dst.copy_(src), 10)
+        ceiling = n / (min(t) * 1e-3) / 1e9
+        best = max(v["gbs"] for v in ce.values())
+        res["ce_device"] = {"by_lanes": ce, "ceiling_one_memcpy_gbs": ceiling, "frac_of_ceiling": best / ceiling,
+                            "slot_steps_per_op": n // w["slot_bytes"]}
+
+    if want("zero_copy") or want("simple_lanes1") or want("posted") or want("ce"):
         del src, dst
 
     if want("loopback"):
@@ -508,6 +535,22 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         ceiling = n / (best * 1e-3) / 1e9
         top = max(v["gbs"] for v in host.values())
         res["host_fifo"] = {"by_lanes": host, "ceiling_concurrent_memcpy_gbs": ceiling, "frac_of_ceiling": top / ceiling}
+        # the same FIFO in proxy mode (shm useMemcpy style): the pump's copy
+        # engines move each slot-step device -> host FIFO -> device
+        f = xp.xp_fifo_create(wh["nchannels"], wh["nslots"], wh["slot_bytes"], xp.XP_PROTO_SIMPLE,
+                              xp.XP_PLACE_HOST_MAPPED)
+        xp.xp_fifo_set_lanes(f, 2)
+        xp.xp_fifo_enable_ce(f)
+        dst.zero_()
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                xp.xp_send_recv_ce(f, src, dst, n, s)
+            t = time_events(torch, s, lambda: xp.xp_send_recv_ce(f, src, dst, n, s), 10)
+        st, _ = xp.xp_fifo_status(f, True)
+        ms = statistics.median(t)
+        res["ce_host_2hops"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "frac_of_ceiling": n / (ms * 1e-3) / 1e9 / ceiling,
+                                "exact": bool(st == 0 and torch.equal(dst, src))}
+        xp.xp_fifo_destroy(f)
         del src, dst, hp, hq, d1, d2
 
     if want("ring"):

@@ -444,7 +444,7 @@ enum { kOpSimple = 0, kOpZeroCopy = 1, kOpPostedCopy = 2, kOpPostedDirect = 3, k
 
 static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream, int mode) {
   const bool zero_copy = mode == kOpZeroCopy;
-  const bool posted = mode >= kOpPostedCopy;
+  const bool posted = mode == kOpPostedCopy || mode == kOpPostedDirect;
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (bytes == 0) return XP_OK;
   if (!src || !dst) return fail(XP_ERR_INVALID, "src or dst is NULL");

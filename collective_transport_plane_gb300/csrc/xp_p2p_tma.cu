@@ -140,7 +140,7 @@ __device__ __forceinline__ void ctl_store(u64* p, u64 v) {
 template <int kMode>
 __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams p) {
   constexpr bool kZeroCopy = kMode == kModeZeroCopy;
-  constexpr bool kPosted = kMode >= kModePostedCopy;
+  constexpr bool kPosted = kMode == kModePostedCopy || kMode == kModePostedDirect;
   constexpr bool kDirect = kMode == kModePostedDirect;
   constexpr bool kToUser = kZeroCopy || kDirect;   // the sender writes dst itself
   constexpr bool kProxy = kMode == kModeProxy;

@@ -3,10 +3,16 @@
 //
 // The sender kernel fills ring 0 (its own send ring) and publishes tail[0] in
 // mapped host memory.  For every channel and hop h this thread watches tail[h]
-// (hop 0) or its own progress on hop h - 1, copies each newly available
-// slot-step from ring h to ring h + 1 with cudaMemcpyAsync on a stream of its
-// own, and publishes tail[h + 1] = step + 1 once the copy's event has
-// completed.  The receiver kernel drains the last ring.  The pump never
+// (hop 0) or its own progress on hop h - 1, copies newly available
+// slot-steps from ring h to ring h + 1 with cudaMemcpyAsync on a stream of
+// its own, and publishes tail[h + 1] = step + 1 once the copy's event has
+// completed.  Consecutive available steps that do not wrap around the ring
+// go in one copy (a run of full slots, possibly ending with a short one), so
+// every ring receives exactly the bytes of one copy per step, with far fewer
+// host calls.  (Measured on the 1 GiB, 16-channel workload: one copy per
+// step 122 GB/s, runs of up to N steps 511 GB/s; capping runs at N/2, N/4 or
+// N/8 steps was slower, 355, 219 and 117 GB/s: host calls, not overlap,
+// bound this mode.)  The receiver kernel drains the last ring.  The pump never
 // decides credit: the sender only fills step s once head >= s + 1 - N, which
 // already implies that every ring's slot s mod N has been read out.
 //
@@ -50,8 +56,10 @@ struct Pump {
   std::atomic<bool> failed{false};
   std::string error;                      // written once before `failed` is set
   std::vector<cudaStream_t> streams;      // [c * hops + h]
-  std::vector<cudaEvent_t> events;        // [(c * hops + h) * N + k]
+  std::vector<cudaEvent_t> events;        // [(c * hops + h) * N + batch % N]
   std::vector<uint64_t> issued, done;     // [c * hops + h], absolute steps
+  std::vector<uint64_t> nb_issued, nb_done;   // [c * hops + h], copies (batches)
+  std::vector<uint64_t> batch_end;        // [(c * hops + h) * N + batch % N]: first step after the batch
 
   char* ctl(int c) const { return cfg.ce_host + (size_t)c * kCeCtlBytes; }
   char* slot(int h, int c, uint64_t step) const {
@@ -74,32 +82,46 @@ struct Pump {
         const int q = c * H + h;
         const uint64_t avail = h == 0 ? load_acquire(ctl(c) + kCeTailOff) : done[q - 1];
         while (issued[q] < avail && issued[q] - done[q] < N) {
-          const uint64_t step = issued[q];
-          const int64_t sz = (int64_t)__atomic_load_n(
-              reinterpret_cast<const uint64_t*>(ctl(c) + kCeSizeOff) + step % N, __ATOMIC_RELAXED);
-          if (sz < 1 || (uint64_t)sz > cfg.slot_bytes) {
-            fail("proxy: channel " + std::to_string(c) + " step " + std::to_string(step) + " has size word " +
-                 std::to_string(sz));
-            return moved;
+          const uint64_t first = issued[q];
+          uint64_t lim = avail < done[q] + N ? avail : done[q] + N;
+          if (lim > first + (N - first % N)) lim = first + (N - first % N);   // no wrap within one copy
+          uint64_t end = first;
+          size_t bytes = 0;
+          while (end < lim) {
+            const int64_t sz = (int64_t)__atomic_load_n(
+                reinterpret_cast<const uint64_t*>(ctl(c) + kCeSizeOff) + end % N, __ATOMIC_RELAXED);
+            if (sz < 1 || (uint64_t)sz > cfg.slot_bytes) {
+              fail("proxy: channel " + std::to_string(c) + " step " + std::to_string(end) + " has size word " +
+                   std::to_string(sz));
+              return moved;
+            }
+            bytes += (size_t)sz;
+            ++end;
+            if ((uint64_t)sz != cfg.slot_bytes) break;   // a short step ends the run
           }
-          cudaError_t e = cudaMemcpyAsync(slot(h + 1, c, step), slot(h, c, step), (size_t)sz, cudaMemcpyDefault,
+          const size_t b = (size_t)q * N + nb_issued[q] % N;
+          cudaError_t e = cudaMemcpyAsync(slot(h + 1, c, first), slot(h, c, first), bytes, cudaMemcpyDefault,
                                           streams[q]);
-          if (e == cudaSuccess) e = cudaEventRecord(events[(size_t)q * N + step % N], streams[q]);
+          if (e == cudaSuccess) e = cudaEventRecord(events[b], streams[q]);
           if (e != cudaSuccess) {
             fail(std::string("proxy: cudaMemcpyAsync: ") + cudaGetErrorString(e));
             return moved;
           }
-          ++issued[q];
+          batch_end[b] = end;
+          ++nb_issued[q];
+          issued[q] = end;
           moved = true;
         }
-        while (done[q] < issued[q]) {
-          const cudaError_t e = cudaEventQuery(events[(size_t)q * N + done[q] % N]);
+        while (nb_done[q] < nb_issued[q]) {
+          const size_t b = (size_t)q * N + nb_done[q] % N;
+          const cudaError_t e = cudaEventQuery(events[b]);
           if (e == cudaErrorNotReady) break;
           if (e != cudaSuccess) {
             fail(std::string("proxy: copy failed: ") + cudaGetErrorString(e));
             return moved;
           }
-          ++done[q];
+          ++nb_done[q];
+          done[q] = batch_end[b];
           store_release(ctl(c) + kCeTailOff + 128 * (h + 1), done[q]);
           moved = true;
         }
@@ -156,6 +178,9 @@ Pump* pump_start(const PumpConfig& cfg, std::string* err) {
   p->events.assign((size_t)Q * cfg.nslots, nullptr);
   p->issued.assign(Q, 0);
   p->done.assign(Q, 0);
+  p->nb_issued.assign(Q, 0);
+  p->nb_done.assign(Q, 0);
+  p->batch_end.assign((size_t)Q * cfg.nslots, 0);
   // counters continue from what the control blocks hold (zero after create or reset)
   for (int c = 0; c < cfg.nchannels; ++c)
     for (int h = 0; h < cfg.hops; ++h)

@@ -143,7 +143,7 @@ def test_ce_needs_enable_and_survives_reset(env):
         dst.zero_()
         xp.xp_fifo_reset(f)           # the pump restarts on zeroed counters
         d = xp.xp_fifo_describe(f, 0)
-        assert not bool(raw_view(torch, d.ce, 2048 // 8, "<u8").any())
+        assert not raw_view(torch, d.ce, 2048 // 8, "<u8").cpu().numpy().any()
     xp.xp_fifo_destroy(f)
     ll = xp.xp_fifo_create(1, 2, 4096, xp.XP_PROTO_LL)
     with pytest.raises(xp.XpError) as e:
