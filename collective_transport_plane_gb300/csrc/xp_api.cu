@@ -181,6 +181,9 @@ xp_status read_status(Common& c, int sync, xp_report* rep) {
 // Cluster co-residency: every cluster of the launch must fit on the GPU.
 std::map<std::tuple<const void*, int, int>, int> g_fits;
 
+// csize > 0: thread-block clusters of csize CTAs, each of which must fit on
+// the GPU.  csize == 0: a cooperative launch without clusters, which the
+// driver runs only if every CTA of the grid is resident at once.
 xp_status launch(const void* kernel, int grid, int block, int csize, void* params, cudaStream_t stream,
                  int smem = 0) {
   cudaLaunchConfig_t cfg = {};
@@ -189,10 +192,15 @@ xp_status launch(const void* kernel, int grid, int block, int csize, void* param
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = csize;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
+  if (csize > 0) {
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = csize;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+  } else {
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+  }
   cfg.attrs = at;
   cfg.numAttrs = 1;
   {
@@ -203,11 +211,21 @@ xp_status launch(const void* kernel, int grid, int block, int csize, void* param
       if (csize > 8) XP_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
       if (smem > 48 * 1024) XP_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
       int n = 0;
-      XP_CUDA(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
+      if (csize > 0) {
+        XP_CUDA(cudaOccupancyMaxActiveClusters(&n, kernel, &cfg));
+      } else {
+        int per_sm = 0, dev = 0, sms = 0;
+        XP_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, (size_t)smem));
+        XP_CUDA(cudaGetDevice(&dev));
+        XP_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        n = per_sm * sms;   // CTAs resident at once
+      }
       it = g_fits.emplace(key, n).first;
     }
-    if (it->second < 1)
+    if (csize > 0 && it->second < 1)
       return fail(XP_ERR_INVALID, "a cluster of %d CTAs x %d threads cannot be resident on this GPU", csize, block);
+    if (csize == 0 && it->second < grid)
+      return fail(XP_ERR_INVALID, "a cooperative grid of %d CTAs does not fit (%d resident at most)", grid, it->second);
   }
   void* args[] = {params};
   XP_CUDA(cudaLaunchKernelExC(&cfg, kernel, args));
@@ -215,6 +233,27 @@ xp_status launch(const void* kernel, int grid, int block, int csize, void* param
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// CTAs of the bulk-copy ring kernel resident on this GPU at once
+int ring_tma_resident() {
+  static std::atomic<int> cached{-1};
+  int v = cached.load();
+  if (v >= 0) return v;
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaFuncSetAttribute(xp::ring_tma_kernel_ptr(XP_F32), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           xp::ring_tma_smem()) != cudaSuccess ||
+      cudaFuncSetAttribute(xp::ring_tma_kernel_ptr(XP_I32), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           xp::ring_tma_smem()) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, xp::ring_tma_kernel_ptr(XP_F32), xp::ring_tma_threads(),
+                                                    (size_t)xp::ring_tma_smem()) != cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;   // unknown: use clusters
+  }
+  v = per_sm * sms;
+  cached.store(v);
+  return v;
+}
 
 // Marks the object's last operation on `st`.  Inside a stream capture the
 // operation becomes a graph node and nothing is recorded (an event recorded
@@ -268,7 +307,7 @@ struct xp_ring {
   int P = 0, C = 0, N = 0;
   size_t S = 0;
   xp_placement place = XP_PLACE_DEVICE;
-  int lanes = 1;
+  int lanes = 0;           // 0: chosen per operation (HBM rings), else CTAs per rank per channel
   Mem mem;
   char* ctl = nullptr;
   char* slots = nullptr;
@@ -599,10 +638,10 @@ xp_status xp_ring_create(int nranks, int nchannels, int nslots, size_t slot_byte
   r->S = slot_bytes;
   r->place = place;
   const int nf = nranks * nchannels;
-  r->ctl_region = round_up((size_t)nf * xp::kCtlBytes, 4096);
+  r->ctl_region = round_up((size_t)nf * xp::kRingMaxLanes * xp::kCtlBytes, 4096);
   r->fifo_stride = round_up((size_t)nslots * slot_bytes, 4096);
   if ((s = common_init(r->cm)) != XP_OK || (s = mem_alloc(r->mem, r->ctl_region + nf * r->fifo_stride, place)) != XP_OK ||
-      (s = mem_init(r->mem, nf)) != XP_OK) {
+      (s = mem_init(r->mem, nf * xp::kRingMaxLanes)) != XP_OK) {
     common_free(r->cm);
     mem_free(r->mem);
     delete r;
@@ -625,7 +664,9 @@ xp_status xp_ring_destroy(xp_ring* r) {
 
 xp_status xp_ring_set_lanes(xp_ring* r, int lanes) {
   if (!r) return fail(XP_ERR_INVALID, "ring is NULL");
-  if (lanes < 1 || r->P * lanes > xp::kMaxCluster) return fail(XP_ERR_INVALID, "nranks * lanes must be <= 16");
+  if (lanes < 0 || lanes > xp::kRingMaxLanes) return fail(XP_ERR_INVALID, "lanes %d not in [0, 4]", lanes);
+  if (r->place != XP_PLACE_DEVICE && r->P * lanes > xp::kMaxCluster)
+    return fail(XP_ERR_INVALID, "host-placed rings need nranks * lanes <= 16");
   r->lanes = lanes;
   return XP_OK;
 }
@@ -656,19 +697,35 @@ xp_status xp_ring_allreduce_virtual(xp_ring* r, const void* const* send_bufs, vo
   p.nranks = r->P;
   p.nchannels = r->C;
   p.nslots = r->N;
-  p.lanes = r->lanes;
+  // lanes 0: HBM rings take the most lanes whose whole grid is resident at
+  // once (a cooperative launch), at least one; host-placed rings take one
+  int lanes = r->lanes;
+  if (lanes == 0) {
+    lanes = 1;
+    if (r->place == XP_PLACE_DEVICE) {
+      const int fit = ring_tma_resident();
+      while (lanes < xp::kRingMaxLanes && r->C * (lanes + 1) * r->P <= fit) ++lanes;
+    }
+  }
+  p.lanes = lanes;
   p.dtype = dt;
   p.slot_bytes = (unsigned)r->S;
   p.status = r->cm.status;
   p.abort_word = g_abort_dev;
   p.timeout_ns = g_timeout_ns.load();
-  const int csize = r->P * r->lanes;
   XP_CUDA(cudaMemsetAsync(r->cm.status, 0, xp::kStatusClearBytes, st));
   if (r->place == XP_PLACE_DEVICE) {
-    // HBM FIFOs: bulk copies through shared memory
-    s = launch(xp::ring_tma_kernel_ptr(dt), r->C * csize, xp::ring_tma_threads(), csize, &p, st, xp::ring_tma_smem());
+    // HBM FIFOs: bulk copies through shared memory, every lane with its own
+    // counters.  The ranks a lane's ring waits on must be resident together:
+    // a cooperative grid when the whole grid fits on the GPU at once (no
+    // cluster placement limits), else one cluster of P CTAs per (channel, lane).
+    const int grid = r->C * lanes * r->P;
+    s = launch(xp::ring_tma_kernel_ptr(dt), grid, xp::ring_tma_threads(), grid <= ring_tma_resident() ? 0 : r->P, &p,
+               st, xp::ring_tma_smem());
   } else {
-    // mapped host FIFOs: 16-byte vector loads and stores from every warp
+    // mapped host FIFOs: 16-byte vector loads and stores from every warp; one
+    // cluster of P * lanes CTAs per channel, lanes sharing the counters
+    const int csize = r->P * lanes;
     s = launch(xp::ring_kernel_ptr(dt), r->C * csize, xp::kRingThreads, csize, &p, st);
   }
   if (s != XP_OK) return s;

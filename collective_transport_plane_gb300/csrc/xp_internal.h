@@ -107,8 +107,12 @@ struct PingParams {
   unsigned long long timeout_ns;
 };
 
+// Ring FIFOs keep kRingMaxLanes control blocks each: lane g of FIFO f (the
+// bulk-copy ring's independent lanes) uses block f * kRingMaxLanes + g.
+constexpr int kRingMaxLanes = 4;
+
 struct RingParams {
-  char* ctl;                      // FIFO (c, r) control block at ctl + (c*nranks + r)*kCtlBytes
+  char* ctl;                      // FIFO (c, r) lane g control block at ctl + ((c*nranks + r)*kRingMaxLanes + g)*kCtlBytes
   char* slots;                    // its slots at slots + (c*nranks + r)*fifo_stride
   unsigned long long fifo_stride;
   const char* send[kMaxRanks];

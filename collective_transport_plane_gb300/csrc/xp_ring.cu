@@ -189,8 +189,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) ring_kernel(const RingParams 
 
   const int f_recv = c * P + r;
   const int f_send = c * P + (r + 1) % P;
-  char* ctl_r = p.ctl + (u64)f_recv * kCtlBytes;
-  char* ctl_s = p.ctl + (u64)f_send * kCtlBytes;
+  char* ctl_r = p.ctl + (u64)f_recv * kRingMaxLanes * kCtlBytes;   // lane block 0: one counter set per FIFO
+  char* ctl_s = p.ctl + (u64)f_send * kRingMaxLanes * kCtlBytes;
   u64* tail_recv = reinterpret_cast<u64*>(ctl_r + kTailOff);
   u64* head_recv = reinterpret_cast<u64*>(ctl_r + kHeadOff);
   u64* base_recv = reinterpret_cast<u64*>(ctl_r + kBaseOff);

@@ -3,11 +3,17 @@
 // Same schedule and FIFO protocol as the vector kernel in xp_ring.cu (ring
 // neighbours from "NCCL transport setup", 具体说明; per round send(r-1),
 // recvReduceSend(r-1-j), recvReduceCopySend(r), recvCopySend(r-1-j),
-// recv(r+1); chunks of at most N/2 slots).  One cluster per channel holds
-// every rank's CTAs (P*G: G lanes per rank); each CTA moves one 16-byte
-// aligned stripe of every slot-step through a ring of kRStages stages of two
-// buffers each (A: received slot, or own input for `send`; B: own input for
-// the reducing steps).  Threads:
+// recv(r+1); chunks of at most N/2 slots).  A channel may be spread over G
+// lanes: lane g moves the g-th 16-byte aligned stripe of every slot-step of
+// every FIFO, with a control block (tail, head, step base) of its own per
+// FIFO, so the lanes of a channel never wait for one another and the element
+// chunking (and with it the order of every sum) does not depend on G.  The
+// ranks a lane's ring waits on must run at once: the grid is launched
+// cooperatively when all of it fits on the GPU, else as one cluster of P CTAs
+// per (channel, lane), co-resident by construction.  Each CTA moves its
+// stripe through a ring of kRStages stages of two buffers each (A: received
+// slot, or own input for `send`; B: own input for the reducing steps).
+// Threads:
 //   loader     - waits for the predecessor's tail (mirrored), bulk-loads the
 //                received slot and/or the own input into a free stage;
 //   compute    - four warps: A += B for recvReduceSend / recvReduceCopySend
@@ -21,14 +27,14 @@
 //                pipeline never drains at a step boundary, and always before
 //                it blocks: what it waits for may depend, around the ring,
 //                on the step it has not reported yet);
-//   signaler   - turns those reports into the cluster-scope release arrive on
-//                the send slot's barrier in the rank's leader CTA (a release
-//                waits for the issuing thread's in-flight traffic: the storer
-//                always has some, the signaler none);
+//   signaler   - turns those reports into the release arrive on the send
+//                slot's barrier (a release waits for the issuing thread's
+//                in-flight traffic: the storer always has some, the signaler
+//                none);
 //   watcher    - mirrors the predecessor's tail and the successor's head into
 //                shared memory;
-//   publishers - in the rank's leader CTA: store the successor FIFO's tail
-//                and the own FIFO's head once all G lanes signalled a step.
+//   publishers - store the successor FIFO's tail and the own FIFO's head (this
+//                lane's control blocks) once the step is signalled.
 #include <cuda_runtime.h>
 
 #include "xp_device.cuh"
@@ -79,9 +85,16 @@ struct Stripe {
   u64 b0, fb, rag, nent;
 };
 
-__device__ __forceinline__ Stripe stripe_of(u64 sz, u64 lanes, u64 lane) {
-  u64 b0, b1;
-  piece(sz, lanes, lane, &b0, &b1);
+// Lane `lane` of `lanes` owns bytes [lane W, (lane + 1) W) of every slot,
+// W = round_up(ceil(S / lanes), 16), whatever the size sz of the slot-step:
+// lanes publish their own counters, so a lane may refill its part of a slot
+// while another lane still reads its own part of the previous step there,
+// and the parts must not depend on the step size.
+__device__ __forceinline__ Stripe stripe_of(u64 sz, u64 slot_bytes, u64 lanes, u64 lane) {
+  const u64 W = ((slot_bytes + lanes - 1) / lanes + 15) & ~15ull;
+  u64 b0 = lane * W, b1 = (lane + 1) * W;
+  if (b0 > sz) b0 = sz;
+  if (b1 > sz) b1 = sz;
   Stripe s;
   s.b0 = b0;
   const u64 n = b1 - b0;
@@ -121,7 +134,7 @@ struct RingWalk {
   }
   __device__ void step_setup() {
     n = (klen - o) < epl ? (klen - o) : epl;
-    st = stripe_of(n * es, G, lane);
+    st = stripe_of(n * es, epl * es, G, lane);
     e = 0;
   }
   __device__ void next_chunk() {
@@ -260,12 +273,13 @@ __global__ void __launch_bounds__(kRThreads, 1) ring_tma_kernel(const RingParams
   const int lane = threadIdx.x & 31;
   const int P = p.nranks;
   const int G = p.lanes;
-  const unsigned crank = cluster_ctarank();
-  const int c = blockIdx.x / (P * G);
-  const int r = (int)crank / G;
-  const int g = (int)crank % G;
-  const unsigned leader = (unsigned)(r * G);
-  const bool leader_cta = crank == leader;
+  // CTA (c, g, r) = block (c * G + g) * P + r: a cooperative grid, or one
+  // cluster of P CTAs per (channel, lane) whose cluster rank is r
+  const int c = (int)(blockIdx.x / P) / G;
+  const int g = (int)(blockIdx.x / P) % G;
+  const int r = (int)(blockIdx.x % P);
+  const unsigned leader = cluster_ctarank();         // every CTA publishes its own lane's counters
+  const bool leader_cta = true;
   const u64 N = (u64)p.nslots;
   const u64 S = p.slot_bytes;
   const u64 es = sizeof(T);
@@ -276,8 +290,8 @@ __global__ void __launch_bounds__(kRThreads, 1) ring_tma_kernel(const RingParams
 
   const int f_recv = c * P + r;
   const int f_send = c * P + (r + 1) % P;
-  char* ctl_r = p.ctl + (u64)f_recv * kCtlBytes;
-  char* ctl_s = p.ctl + (u64)f_send * kCtlBytes;
+  char* ctl_r = p.ctl + ((u64)f_recv * kRingMaxLanes + g) * kCtlBytes;
+  char* ctl_s = p.ctl + ((u64)f_send * kRingMaxLanes + g) * kCtlBytes;
   u64* tail_recv = reinterpret_cast<u64*>(ctl_r + kTailOff);
   u64* head_recv = reinterpret_cast<u64*>(ctl_r + kHeadOff);
   u64* base_recv = reinterpret_cast<u64*>(ctl_r + kBaseOff);
@@ -318,8 +332,8 @@ __global__ void __launch_bounds__(kRThreads, 1) ring_tma_kernel(const RingParams
     }
     if (leader_cta) {
       for (int k = 0; k < p.nslots; ++k) {
-        mbar_init(smem_addr(&bars_send[k]), (uint32_t)G);
-        mbar_init(smem_addr(&bars_recv[k]), (uint32_t)G);
+        mbar_init(smem_addr(&bars_send[k]), 1u);
+        mbar_init(smem_addr(&bars_recv[k]), 1u);
       }
     }
     mbar_init_fence();

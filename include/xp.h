@@ -261,13 +261,25 @@ xp_status xp_ll_pingpong(xp_fifo* ab, xp_fifo* ba, int iters, uint64_t* elapsed_
 /* Create the FIFOs of a virtual ring of `nranks` ranks in this GPU's memory
  * ([setup] 具体说明: rank r receives from r-1 and sends to r+1): for each
  * rank and channel one SIMPLE FIFO of nslots x slot_bytes owned by the
- * receiving rank.  2 <= nranks, nranks * lanes <= 16 (one cluster per
- * channel), 2 <= nslots <= 64, slot_bytes a non-zero multiple of 16. */
+ * receiving rank.  2 <= nranks <= 16 (the ranks of a channel share one
+ * cluster), 1 <= nchannels <= 64, 2 <= nslots <= 64, slot_bytes a non-zero
+ * multiple of 16. */
 xp_status xp_ring_create(int nranks, int nchannels, int nslots, size_t slot_bytes, xp_placement place,
                          xp_ring** out);
 xp_status xp_ring_destroy(xp_ring* r);
 
-/* CTAs per rank per channel (1 <= lanes, nranks * lanes <= 16; default 1). */
+/* CTAs per rank per channel (0 <= lanes <= 4; default 0).  0 = chosen at
+ * each operation: for an HBM ring the largest lane count (at most 4) whose
+ * whole grid of nchannels * lanes * nranks CTAs is resident on the GPU at
+ * once, at least 1; for a host-placed ring 1.  HBM rings: lane g
+ * moves the g-th 16-byte aligned stripe of every slot-step of every FIFO,
+ * with a control block of its own per FIFO (the lanes of a channel are
+ * independent rings over disjoint stripes; the result does not depend on
+ * the lane count).  The ranks of a lane's ring must run at once: a grid
+ * that is resident as a whole is launched cooperatively, a larger one as one
+ * cluster of nranks CTAs per channel and lane.
+ * Host-placed rings: the lanes of a rank share its counters, one cluster of
+ * nranks * lanes CTAs per channel, so nranks * lanes <= 16. */
 xp_status xp_ring_set_lanes(xp_ring* r, int lanes);
 
 /* Allreduce (sum) of `count` elements of type dt (XP_F32 or XP_I32) over the

@@ -70,28 +70,45 @@ def test_ring_in_place_and_repeated(env):
     xp.xp_ring_destroy(ring)
 
 
-def test_ring_two_lanes(env):
+@pytest.mark.parametrize("lanes", [2, 3, 4])
+@pytest.mark.parametrize("P,n,nchan,nslots,slot", [(8, (1 << 18) + 5, 2, 8, 4096), (3, 100003, 3, 4, 1024),
+                                                   (5, 77, 2, 2, 16)])
+def test_ring_lanes(env, lanes, P, n, nchan, nslots, slot):
+    # lanes split every slot-step into stripes with counters of their own:
+    # the result is the same ring-order sum for any lane count
     torch, xp = env
-    xs = _inputs(8, 1 << 18, "f32")
-    want = oracle.ring_order_sum(xs, 2, 8, 4096)
-    try:
-        res = _ring(torch, xp, xs, 2, 8, 4096, lanes=2)
-    except xp.XpError as e:
-        if e.status == xp.XP_ERR_INVALID:
-            pytest.skip(f"16-CTA clusters not available: {e}")
-        raise
-    for got in res:
-        assert np.array_equal(got, want)
+    for dtype in ("f32", "i32"):
+        xs = _inputs(P, n, dtype, seed_base=lanes)
+        want = oracle.ring_order_sum(xs, nchan, nslots, slot)
+        for got in _ring(torch, xp, xs, nchan, nslots, slot, lanes=lanes):
+            assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "i32"])
-def test_ring_workload(env, dtype):
-    # 8 ranks x 256 MiB, 8 channels of 8 x 512 KiB per rank-FIFO
+def test_ring_lanes_repeated_and_host_placed(env):
+    # counters of every lane carry over between operations; host-placed rings
+    # share one counter set among a rank's lanes
+    torch, xp = env
+    P, n, nchan, nslots, slot = 4, 54321, 2, 4, 2048
+    for place in (0, 1):
+        ring = xp.xp_ring_create(P, nchan, nslots, slot, place)
+        for i, lanes in enumerate((2, 1, 3, 2)):
+            xp.xp_ring_set_lanes(ring, lanes)
+            xs = _inputs(P, n, "f32", seed_base=40 + i)
+            want = oracle.ring_order_sum(xs, nchan, nslots, slot)
+            for got in _ring(torch, xp, xs, nchan, nslots, slot, ring=ring):
+                assert np.array_equal(got, want)
+        xp.xp_ring_destroy(ring)
+
+
+@pytest.mark.parametrize("dtype,lanes", [("f32", 1), ("i32", 1), ("f32", 0), ("i32", 0)])
+def test_ring_workload(env, dtype, lanes):
+    # 8 ranks x 256 MiB, 8 channels of 8 x 512 KiB per rank-FIFO; lanes 0 lets
+    # the library pick (two lanes, a cooperative grid of 128 CTAs)
     torch, xp = env
     w = workloads.RING
     xs = _inputs(w["nranks"], w["nelems"], dtype, w["seed_base"])
     want = oracle.ring_order_sum(xs, w["nchannels"], w["nslots"], w["slot_bytes"])
-    for got in _ring(torch, xp, xs, w["nchannels"], w["nslots"], w["slot_bytes"]):
+    for got in _ring(torch, xp, xs, w["nchannels"], w["nslots"], w["slot_bytes"], lanes=lanes):
         assert np.array_equal(got, want)
 
 
