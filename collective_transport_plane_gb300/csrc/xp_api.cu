@@ -300,6 +300,9 @@ struct xp_fifo {
   char* recv_ring = nullptr;
   int hops = 0;
   xp::Pump* pump = nullptr;
+  // staged (host -> device -> FIFO -> device -> host) transfers, made on first use
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
 };
 
 struct xp_ring {
@@ -387,6 +390,10 @@ xp_status xp_fifo_destroy(xp_fifo* f) {
   if (!f) return XP_OK;
   cudaDeviceSynchronize();
   xp::pump_stop(f->pump);
+  for (cudaEvent_t e : f->ev)
+    if (e) cudaEventDestroy(e);
+  if (f->s_in) cudaStreamDestroy(f->s_in);
+  if (f->s_out) cudaStreamDestroy(f->s_out);
   common_free(f->cm);
   mem_free(f->mem);
   mem_free(f->ce_mem);
@@ -559,6 +566,47 @@ xp_status xp_send_recv_posted(xp_fifo* f, const void* src, void* dst, size_t byt
 
 xp_status xp_send_recv_ce(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream) {
   return p2p_op(f, src, dst, bytes, stream, kOpProxy);
+}
+
+xp_status xp_send_recv_staged(xp_fifo* f, const void* host_src, void* host_dst, void* dev_src, void* dev_dst,
+                              size_t bytes, size_t chunk_bytes, xp_stream_t stream) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  if (bytes == 0) return XP_OK;
+  if (!host_src || !host_dst || !dev_src || !dev_dst) return fail(XP_ERR_INVALID, "a buffer is NULL");
+  if (chunk_bytes == 0) chunk_bytes = (size_t)64 << 20;
+  if (chunk_bytes % 16) return fail(XP_ERR_INVALID, "chunk_bytes %zu is not a multiple of 16", chunk_bytes);
+  if (f->proto == XP_PROTO_LL && bytes % 8) return fail(XP_ERR_INVALID, "LL moves whole 8-byte lines: bytes %% 8 != 0");
+  xp_status s = check_device(f->cm);
+  if (s != XP_OK) return s;
+  if (!f->s_in) {
+    XP_CUDA(cudaStreamCreateWithFlags(&f->s_in, cudaStreamNonBlocking));
+    XP_CUDA(cudaStreamCreateWithFlags(&f->s_out, cudaStreamNonBlocking));
+    for (cudaEvent_t& e : f->ev) XP_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // everything starts after the work already on `stream`
+  XP_CUDA(cudaEventRecord(f->ev[0], st));
+  XP_CUDA(cudaStreamWaitEvent(f->s_in, f->ev[0], 0));
+  XP_CUDA(cudaStreamWaitEvent(f->s_out, f->ev[0], 0));
+  const char* hs = static_cast<const char*>(host_src);
+  char* hd = static_cast<char*>(host_dst);
+  char* ds = static_cast<char*>(dev_src);
+  char* dd = static_cast<char*>(dev_dst);
+  for (size_t off = 0; off < bytes; off += chunk_bytes) {
+    const size_t n = bytes - off < chunk_bytes ? bytes - off : chunk_bytes;
+    // chunk i: copy in on s_in | transfer on `stream` | copy out on s_out;
+    // each event is waited on right after it is recorded, so two suffice
+    XP_CUDA(cudaMemcpyAsync(ds + off, hs + off, n, cudaMemcpyHostToDevice, f->s_in));
+    XP_CUDA(cudaEventRecord(f->ev[1], f->s_in));
+    XP_CUDA(cudaStreamWaitEvent(st, f->ev[1], 0));
+    if ((s = p2p_op(f, ds + off, dd + off, n, stream, kOpSimple)) != XP_OK) return s;
+    XP_CUDA(cudaEventRecord(f->ev[2], st));
+    XP_CUDA(cudaStreamWaitEvent(f->s_out, f->ev[2], 0));
+    XP_CUDA(cudaMemcpyAsync(hd + off, dd + off, n, cudaMemcpyDeviceToHost, f->s_out));
+  }
+  XP_CUDA(cudaEventRecord(f->ev[0], f->s_out));
+  XP_CUDA(cudaStreamWaitEvent(st, f->ev[0], 0));
+  return record_done(f->cm, st);
 }
 
 xp_status xp_fifo_status(xp_fifo* f, int sync, xp_report* report) {

@@ -28,7 +28,7 @@ EXPORTS = [
     "xp_ring_destroy", "xp_ring_set_lanes", "xp_ring_allreduce_virtual", "xp_ring_status", "xp_ring_reset",
     "xp_set_spin_timeout_ns", "xp_abort", "xp_status_string", "xp_last_error", "xp_version",
     "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes", "xp_send_recv_posted", "xp_fifo_enable_ce",
-    "xp_send_recv_ce",
+    "xp_send_recv_ce", "xp_send_recv_staged",
 ]
 
 
@@ -67,6 +67,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         "xp_send_recv_posted": [P, P, P, Z, I, P],
         "xp_fifo_enable_ce": [P],
         "xp_send_recv_ce": [P, P, P, Z, P],
+        "xp_send_recv_staged": [P, P, P, P, P, Z, Z, P],
         "xp_fifo_status": [P, I, ctypes.POINTER(xp_report)],
         "xp_fifo_reset": [P],
         "xp_ll_pingpong": [P, P, I, ctypes.POINTER(U64), P],
@@ -168,6 +169,12 @@ def xp_fifo_enable_ce(fifo: int) -> None:
 
 def xp_send_recv_ce(fifo: int, src, dst, nbytes: int, stream=None) -> None:
     _check(_lib.xp_send_recv_ce(fifo, _ptr(src), _ptr(dst), nbytes, _stream(stream)), "xp_send_recv_ce")
+
+
+def xp_send_recv_staged(fifo: int, host_src, host_dst, dev_src, dev_dst, nbytes: int, chunk_bytes: int = 0,
+                        stream=None) -> None:
+    _check(_lib.xp_send_recv_staged(fifo, _ptr(host_src), _ptr(host_dst), _ptr(dev_src), _ptr(dev_dst), nbytes,
+                                    chunk_bytes, _stream(stream)), "xp_send_recv_staged")
 
 
 def xp_send_recv_posted(fifo: int, src, dst, nbytes: int, direct: bool = False, stream=None) -> None:

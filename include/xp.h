@@ -240,6 +240,23 @@ xp_status xp_fifo_enable_ce(xp_fifo* f);
  * them on the FIFO. */
 xp_status xp_send_recv_ce(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream);
 
+/* xp_send_recv from host memory to host memory, staged through device
+ * buffers the caller owns.  The pages have no counterpart: it is the
+ * end-to-end form of a transfer, for callers whose data lives on the host.
+ * host_src / host_dst should be pinned (cudaHostAlloc or registered), else the
+ * copies are not asynchronous; dev_src / dev_dst are device buffers of `bytes`
+ * bytes, 16-byte aligned, not overlapping.  The buffer is cut into chunks of
+ * chunk_bytes (0 = 64 MiB; a multiple of 16); chunk i is copied host ->
+ * device on a stream of the FIFO's own, moved by one xp_send_recv on
+ * `stream`, and copied device -> host on a second stream of the FIFO's own,
+ * so the two copy directions and the transfers of neighbouring chunks
+ * overlap.  Everything starts after the work already on `stream`, and
+ * `stream` waits for the last copy out: the call is asynchronous on `stream`
+ * like the others.  Errors as xp_send_recv; a device error in one chunk makes
+ * the later chunks refuse (xp_fifo_status then reports XP_ERR_ABORTED). */
+xp_status xp_send_recv_staged(xp_fifo* f, const void* host_src, void* host_dst, void* dev_src, void* dev_dst,
+                              size_t bytes, size_t chunk_bytes, xp_stream_t stream);
+
 /* Outcome of the FIFO's last operation.  sync != 0 first waits for the
  * FIFO's last stream; sync == 0 reads whatever the device has written so far
  * (XP_OK if the operation is still running without error).  `report` may be
