@@ -375,7 +375,7 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
     if want("zero_copy"):
         # zero copy, 1 GiB through the same geometry
         zc = {}
-        for lanes in (4, 8):
+        for lanes in (8, 12):
             f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
             xp.xp_fifo_set_lanes(f, lanes)
             with torch.cuda.stream(s):
@@ -406,7 +406,7 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         # staging slots (4 bytes of HBM traffic per payload byte) and direct
         # mode into dst (2 bytes per payload byte)
         posted = {}
-        for direct, lanes, rl in ((False, 6, 7), (True, 8, None)):
+        for direct, lanes, rl in ((False, 6, 7), (True, 12, None)):
             f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
             xp.xp_fifo_set_lanes(f, lanes)
             if rl:

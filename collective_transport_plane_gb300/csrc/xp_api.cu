@@ -453,9 +453,9 @@ xp_status xp_fifo_enable_ce(xp_fifo* f) {
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
-  if (lanes < 1 || lanes > 8) return fail(XP_ERR_INVALID, "lanes %d not in [1, 8]", lanes);
+  if (lanes < 1 || lanes > xp::kMaxCluster - 1) return fail(XP_ERR_INVALID, "lanes %d not in [1, 15]", lanes);
   f->lanes = lanes;
-  f->rlanes = lanes;
+  f->rlanes = lanes <= xp::kMaxCluster / 2 ? lanes : xp::kMaxCluster - lanes;
   return XP_OK;
 }
 
@@ -534,6 +534,8 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     p.lanes = f->lanes;
     p.rlanes = (zero_copy || mode == kOpPostedDirect) ? 1 : f->rlanes;
     csize = p.lanes + p.rlanes;
+    if (csize > xp::kMaxCluster)
+      return fail(XP_ERR_INVALID, "%d sender + %d receiver CTAs per channel exceed a cluster of 16", p.lanes, p.rlanes);
     if (f->place == XP_PLACE_DEVICE || mode == kOpProxy) {
       // HBM FIFO (or the proxy mode's device rings): bulk copies through shared memory
       kernel = xp::p2p_tma_kernel_ptr(mode);

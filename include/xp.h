@@ -149,10 +149,13 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
 xp_status xp_fifo_destroy(xp_fifo* f);
 
 /* CTAs per channel side: each channel's sender and receiver are each spread
- * over `lanes` CTAs of one thread-block cluster that share the channel's one
- * tail and one head (1 <= lanes <= 8; default 1: one sender CTA and one
- * receiver CTA per channel).  Sets both sides.  SIMPLE FIFOs only.  Takes
- * effect at the next operation. */
+ * over CTAs of one thread-block cluster that share the channel's one tail and
+ * one head (default 1: one sender CTA and one receiver CTA per channel).
+ * Sets the sender side to `lanes` (1 <= lanes <= 15) and the receiver side to
+ * min(lanes, 16 - lanes); zero copy and direct posted transfers use one
+ * receiver CTA, so up to 15 sender lanes serve them.  An operation whose
+ * sender + receiver CTAs exceed 16 is refused (XP_ERR_INVALID).  SIMPLE FIFOs
+ * only.  Takes effect at the next operation. */
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
 
 /* Receiver CTAs per channel of xp_send_recv, independently of the sender's

@@ -206,3 +206,34 @@ def test_simple_receiver_lanes(env, n, nchan, nslots, slot, lanes, rlanes, place
         got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, fifo=fifo)
         assert np.array_equal(got, want)
     xp.xp_fifo_destroy(fifo)
+
+
+@pytest.mark.parametrize("mode", ["simple", "zero_copy", "posted_copy", "posted_direct"])
+def test_wide_sender_lanes(env, mode):
+    # 12 sender lanes: SIMPLE and copy-mode posts pair them with 4 receiver
+    # lanes (a 16-CTA cluster), zero copy and direct posts with one
+    torch, xp = env
+    src_np = workloads.uniform_bytes((3 << 20) + 4099, seed=12)
+    nchan, nslots, slot = 5, 4, 65536
+    f = xp.xp_fifo_create(nchan, nslots, slot)
+    xp.xp_fifo_set_lanes(f, 12)
+    src = to_dev(torch, src_np)
+    dst = torch.zeros_like(src)
+    s = torch.cuda.current_stream()
+    if mode == "simple":
+        want = oracle.simple_transfer(src_np, nchan, nslots, slot, seed=2)[0]
+        xp.xp_send_recv(f, src, dst, src_np.nbytes, s)
+    elif mode == "zero_copy":
+        want = oracle.zero_copy_transfer(src_np, nchan, nslots, slot, seed=2)[0]
+        xp.xp_send_recv_zero_copy(f, src, dst, src_np.nbytes, s)
+    else:
+        direct = mode == "posted_direct"
+        want = oracle.posted_transfer(src_np, nchan, nslots, slot, seed=2, direct=direct)[0]
+        xp.xp_send_recv_posted(f, src, dst, src_np.nbytes, direct, s)
+    st, rep = xp.xp_fifo_status(f, True)
+    assert st == xp.XP_OK, (st, rep.where)
+    assert np.array_equal(from_dev(dst), want)
+    assert xp.xp_fifo_describe(f, 0).recv_lanes == 4
+    with pytest.raises(xp.XpError):
+        xp.xp_fifo_set_recv_lanes(f, 5)           # 12 + 5 > 16
+    xp.xp_fifo_destroy(f)
