@@ -75,3 +75,27 @@ def test_ll_early_credit_is_caught():
 def test_ll_skipped_credit_is_caught():
     with pytest.raises(ProtocolViolation):
         explore(_ll_system(3, 1, 1, send_fault="skip_credit"), _ll_final)
+
+
+def test_ll_flags_wrap_at_32_bits():
+    # step counters are 64-bit, flags (step + 1) mod 2^32: a run that starts
+    # with every slot used once below the wrap crosses it intact, and the
+    # step whose flag is 0 reads its own lines, not the zeroed memory
+    N, S = 4, 64
+    B = (1 << 32) - 2 * N - 3
+    words = np.random.default_rng(7).integers(0, 2 ** 32, 1000, dtype=np.uint32)
+    out, fifos, _ = oracle.ll_transfer(words, 2, N, S, seed=4, fifos=[LLFifo(N, S, step0=B) for _ in range(2)])
+    assert np.array_equal(out, words)
+    assert ll_flag((1 << 32) - 1) == 0 and all(f.head > (1 << 32) for f in fifos)
+
+
+def test_ll_zero_flag_on_unwritten_slot_is_caught():
+    # an unreachable start: the very first use of a slot expects flag 0, which
+    # zeroed memory matches; the checker must refuse the stale lines
+    N, S = 1, 16
+    f = LLFifo(N, S, step0=(1 << 32) - 1)
+    words = np.arange(1, 5, dtype=np.uint32)
+    out = np.zeros_like(words)
+    with pytest.raises(ProtocolViolation):
+        explore(lambda: System([LLSender(f, words, 0, 4), LLReceiver(f, out, 0, 4)], [f], [out]),
+                lambda s: None)
