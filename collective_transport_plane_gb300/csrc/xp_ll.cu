@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
 
 // Ping-pong: CTA 0 (A) sends one line through `ab`, CTA 1 (B) answers
 // through `ba`; `iters` round trips between two globaltimer reads.  Each
-// side is the receiver of one FIFO and returns its head after every line.
+// side is the receiver of one FIFO and returns its head for every line.
 __global__ void __launch_bounds__(32, 1) ll_pingpong_kernel(const PingParams p) {
   const unsigned crank = cluster_ctarank();
   const WaitCtx w{p.status, p.abort_word, p.timeout_ns, (int)crank};
@@ -166,18 +166,25 @@ __global__ void __launch_bounds__(32, 1) ll_pingpong_kernel(const PingParams p) 
         report(w, XP_ERR_BOUNDS, XP_WAIT_LL_FLAG, a, i);
         return false;
       }
-      st_release(rhead, r + 1);
       return true;
     };
+    // Credit for line i goes back after the next line is sent: the release
+    // orders this thread's memory traffic and would delay the reply if it
+    // came first (measured: 1067 ns one way with it in front, 698 ns after).
+    auto pub = [&](u64 i) { st_release(rhead, rbase + i + 1); };
 
     const u64 iters = (u64)p.iters;
     const u64 t0 = globaltimer();
     u64 i = 0;
     for (; i < iters; ++i) {
       if (is_a) {
-        if (!send_line(i) || !recv_line(i)) break;
+        if (!send_line(i)) break;
+        if (i > 0) pub(i - 1);
+        if (!recv_line(i)) break;
+        if (i + 1 == iters) pub(i);
       } else {
         if (!recv_line(i) || !send_line(i)) break;
+        pub(i);
       }
     }
     const u64 t1 = globaltimer();
