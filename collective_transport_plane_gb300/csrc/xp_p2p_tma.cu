@@ -1,10 +1,11 @@
-// SIMPLE and zero-copy channel kernels for FIFOs in HBM, data moved with bulk
-// (TMA) copies through shared memory.
+// Channel kernel for FIFOs in HBM, data moved with bulk (TMA) copies through
+// shared memory: SIMPLE, zero copy, receiver-driven credit (copy and direct
+// modes) and the proxy (copy-engine) mode, one template instance each.
 //
 // Cluster layout as in the vector kernels (xp_p2p.cu): per channel, CTAs
-// [0, G) send and [G, G + GR) receive (zero copy: CTA G receives).  Each CTA moves
-// one contiguous stripe of every slot-step ("lane") through a ring of
-// kTmaStages shared-memory stages:
+// [0, G) send and [G, G + GR) receive (zero copy and direct posts: CTA G
+// receives).  Each CTA moves one contiguous stripe of every slot-step
+// ("lane") through a ring of kTmaStages shared-memory stages:
 //   sender    - one mover thread issues bulk loads from src up to kLookSend
 //               entries ahead (they need nothing) and bulk stores into the
 //               slot (they need credit);
@@ -13,22 +14,25 @@
 //               and frees it, so neither stream waits for the other's
 //               memory latency;
 //   watcher   - polls the one remote counter the CTA waits on (sender: head,
-//               receiver: tail) and mirrors it into shared memory, so no
-//               copying thread stalls on a global-memory round trip;
-//   publisher - in the side's leader CTA only: waits until all G lanes have
+//               or the posts; receiver: tail, or the completions) and
+//               mirrors it into shared memory, so no copying thread stalls on
+//               a global-memory round trip;
+//   publisher - in the side's leader CTA only: waits until all lanes have
 //               signalled a slot-step on its mbarrier and publishes the one
 //               channel-wide counter (tail = step + 1 on the sender side,
-//               head = step + 1 on the receiver side).
+//               head = step + 1 on the receiver side; posted modes: the
+//               completion, or the next post).
 // A sender stripe is signalled once its bulk stores have completed.  The mover
 // checks that only after kDefer stores of the next step are in flight, so the
 // store pipeline never drains at a step boundary, and before it blocks on
 // credit it reports whatever is pending (a FIFO of one slot would otherwise
 // wait on itself).  It reports through shared memory to a signaler thread,
 // which does the cluster-scope release arrive: a release waits for the
-// issuing thread's in-flight memory traffic, and the mover always has some.  A receiver stripe is signalled as soon as its
-// bulk loads from the slot have landed in shared memory.  Slot traffic is
-// marked evict_last in L2 and user-buffer traffic evict_first, so the FIFO
-// stays L2-resident while src and dst stream through.
+// issuing thread's in-flight memory traffic, and the mover always has some.
+// A receiver stripe is signalled as soon as its bulk loads from the slot have
+// landed in shared memory.  Slot traffic is marked evict_last in L2 and
+// user-buffer traffic evict_first, so the FIFO stays L2-resident while src
+// and dst stream through.
 #include <cuda_runtime.h>
 
 #include "xp_device.cuh"
