@@ -57,9 +57,14 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the timed kernel's sources with comments and whitespace removed,
+    so that only a change of code makes a committed ncu capture stale."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "collective_transport_plane_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "collective_transport_plane_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
