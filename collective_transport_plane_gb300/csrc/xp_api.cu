@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -34,7 +35,17 @@ using xp::DevStatus;
 namespace {
 
 thread_local std::string g_err;
-std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+// Spin timeout of device waits; XP_SPIN_TIMEOUT_NS in the environment sets the
+// starting value (1e3 .. 6e10 ns), xp_set_spin_timeout_ns changes it.
+unsigned long long initial_timeout_ns() {
+  const char* e = getenv("XP_SPIN_TIMEOUT_NS");
+  if (!e || !*e) return 2000000000ull;
+  char* end = nullptr;
+  const unsigned long long v = strtoull(e, &end, 10);
+  if (*end || v < 1000ull || v > 60000000000ull) return 2000000000ull;
+  return v;
+}
+std::atomic<unsigned long long> g_timeout_ns{initial_timeout_ns()};
 std::mutex g_mu;
 int* g_abort_host = nullptr;
 int* g_abort_dev = nullptr;
@@ -290,6 +301,7 @@ struct xp_fifo {
   char* ctl = nullptr;     // device view
   char* slots = nullptr;   // device view
   char* pctl = nullptr;    // device view: posted-FIFO blocks
+  xp::ChanStats* stats = nullptr;   // device: one record per channel
   size_t ctl_region = 0;
   size_t pctl_region = 0;
   size_t ch_stride = 0;
@@ -379,6 +391,14 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
     delete f;
     return s;
   }
+  if (cudaMalloc(reinterpret_cast<void**>(&f->stats), (size_t)nchannels * sizeof(xp::ChanStats)) != cudaSuccess ||
+      cudaMemset(f->stats, 0, (size_t)nchannels * sizeof(xp::ChanStats)) != cudaSuccess) {
+    if (f->stats) cudaFree(f->stats);
+    common_free(f->cm);
+    mem_free(f->mem);
+    delete f;
+    return fail(XP_ERR_CUDA, "allocating the channel records failed");
+  }
   f->ctl = f->mem.dev;
   f->pctl = f->mem.dev + f->ctl_region;
   f->slots = f->pctl + f->pctl_region;
@@ -396,6 +416,7 @@ xp_status xp_fifo_destroy(xp_fifo* f) {
   if (f->s_out) cudaStreamDestroy(f->s_out);
   common_free(f->cm);
   mem_free(f->mem);
+  if (f->stats) cudaFree(f->stats);
   mem_free(f->ce_mem);
   mem_free(f->ring_mem);
   delete f;
@@ -507,6 +528,7 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   xp::P2pParams p = {};
   p.ctl = f->ctl;
+  p.stats = f->stats;
   p.pctl = f->pctl;
   p.ce = f->ce_mem.dev;
   p.send_ring = f->send_ring;
@@ -616,6 +638,21 @@ xp_status xp_fifo_status(xp_fifo* f, int sync, xp_report* report) {
   const xp_status s = read_status(f->cm, sync, report);
   if (const char* e = xp::pump_error(f->pump)) xp::set_last_error(e);
   return s;
+}
+
+xp_status xp_fifo_stats(xp_fifo* f, int channel, xp_channel_stats* out) {
+  if (!f || !out) return fail(XP_ERR_INVALID, "NULL argument");
+  if (channel < 0 || channel >= f->C) return fail(XP_ERR_INVALID, "channel %d out of range", channel);
+  if (f->cm.used) XP_CUDA(cudaEventSynchronize(f->cm.done));
+  xp::ChanStats h;
+  XP_CUDA(cudaMemcpyAsync(&h, f->stats + channel, sizeof h, cudaMemcpyDeviceToHost, f->cm.query));
+  XP_CUDA(cudaStreamSynchronize(f->cm.query));
+  out->steps = h.steps;
+  out->t_start_ns = h.t_start;
+  out->t_end_ns = h.t_end;
+  out->send_polls = h.send_polls;
+  out->recv_polls = h.recv_polls;
+  return XP_OK;
 }
 
 xp_status xp_fifo_reset(xp_fifo* f) {

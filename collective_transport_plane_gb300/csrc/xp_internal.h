@@ -68,8 +68,23 @@ struct DevStatus {
 static_assert(sizeof(DevStatus) == 128, "status block layout");
 constexpr int kStatusClearBytes = 64;
 
+// Per-channel record of the last operation (device memory, one per channel),
+// written by the channel kernel: slot-steps moved, device time (globaltimer)
+// when the sender side started and when the receiver side published its last
+// step, and how many times each side's watcher polled its remote counter.
+struct ChanStats {
+  unsigned long long steps;
+  unsigned long long t_start;
+  unsigned long long t_end;
+  unsigned long long send_polls;
+  unsigned long long recv_polls;
+  unsigned long long pad[3];
+};
+static_assert(sizeof(ChanStats) == 64, "stats record layout");
+
 struct P2pParams {
   char* ctl;                      // nchannels control blocks
+  ChanStats* stats;               // nchannels records, or nullptr
   char* pctl;                     // nchannels posted-FIFO blocks (posted transfers)
   char* ce;                       // nchannels proxy-mode blocks (mapped host memory)
   char* send_ring;                // proxy mode: the sender's own slots, same geometry as `slots`

@@ -55,6 +55,14 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
   cluster_sync_all();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
+  ChanStats* cs = p.stats ? p.stats + ch : nullptr;
+  if (cs && sender && threadIdx.x == 0) {
+    const u64 t = globaltimer();
+    cs->steps = run ? nsteps : 0;
+    cs->t_start = t;
+    cs->send_polls = cs->recv_polls = 0;
+    if (!run) cs->t_end = t;
+  }
   const u64 T = 32ull * kCopyWarps;
   const u64 tid = threadIdx.x;
 
@@ -115,6 +123,7 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
       st_release(head, step + 1);
     }
     if (r == nsteps) st_relaxed(basew, base + nsteps);
+    if (cs) cs->t_end = globaltimer();
   }
   __syncwarp();
   cluster_sync_all();

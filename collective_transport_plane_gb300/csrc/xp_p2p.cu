@@ -74,6 +74,14 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
   cluster_sync_all();   // barriers initialised before any remote arrive
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
+  ChanStats* cs = p.stats ? p.stats + ch : nullptr;
+  if (cs && sender && leader_cta && threadIdx.x == 0) {
+    const u64 t = globaltimer();
+    cs->steps = run ? nsteps : 0;
+    cs->t_start = t;
+    cs->send_polls = cs->recv_polls = 0;
+    if (!run) cs->t_end = t;
+  }
 
   if (run && warp < kCopyWarps) {
     const u64 parts = (u64)GS * kCopyWarps;
@@ -139,6 +147,7 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
         }
         if (j == nsteps) st_relaxed(basew, base + nsteps);
       }
+      if (cs) cs->t_end = globaltimer();
     } else if (leader_cta) {
       u64 s = 0;
       unsigned max_occ = 0;
@@ -168,6 +177,7 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
       } else if (s == nsteps) {
         st_relaxed(basew, base + nsteps);
       }
+      if (cs && !sender) cs->t_end = globaltimer();
     }
   }
 done:

@@ -229,6 +229,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   cluster_sync_all();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
+  ChanStats* cs = p.stats ? p.stats + ch : nullptr;
+  if (cs && sender && leader_cta && threadIdx.x == 0) {
+    const u64 t = globaltimer();
+    cs->steps = run ? nsteps : 0;
+    cs->t_start = t;
+    cs->send_polls = 0;
+    cs->recv_polls = 0;
+    if (!run) cs->t_end = t;
+  }
   const uint32_t sm0 = smem_addr(stage_mem);
   const uint32_t bar0 = map_to_rank(smem_addr(&bars[0]), leader);
   const u64 pol_slot = policy_evict_last();     // FIFO slots: reused every N steps
@@ -257,6 +266,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
             st_release(head, base + j + 1);
           }
           if (j == nsteps) st_relaxed(basew, base + nsteps);
+          if (cs) cs->t_end = globaltimer();
         }
       } else if (warp == 1 && kDirect) {
         // direct-posted receiver: keep up to N posts of dst outstanding,
@@ -278,6 +288,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           if (j + N < nsteps) post(j + N);
         }
         if (j == nsteps) st_relaxed(basew, base + nsteps);
+        if (cs) cs->t_end = globaltimer();
       }
     } else if (warp == 0) {
       Entries en;
@@ -456,13 +467,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       // in shared memory and mirrors the count; receiver (copy mode): takes
       // the completions in order, checks their sizes and mirrors the count
       WaitClock clk;
+      u64 polls = 0;
       for (u64 m = 0; m < nsteps; ++m) {
         const u64 k = (base + m) % N;
         const u64* idx = sender ? posts + 8 * k + 2 : cq + 2 * k + 1;
         const u64 want = base + m + 1;
         u64 v;
         bool ok = true;
-        while ((v = ld_acquire(idx)) < want) {
+        while (++polls, (v = ld_acquire(idx)) < want) {
           if (!clk.tick(w, sender ? XP_WAIT_POST : XP_WAIT_COMPLETION, v, want)) { ok = false; break; }
         }
         if (!ok) break;
@@ -483,15 +495,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         st_release_cta_shared(&s_mirror, want);
         clk = WaitClock();   // the timeout counts time without progress
       }
+      if (cs && leader_cta) (sender ? cs->send_polls : cs->recv_polls) = polls;
     } else if (warp == 2) {
       // ---------------- watcher ----------------
       // sender: head, as far as the last step's credit needs it;
       // receiver: tail, up to the last step
       const u64* word = sender ? head : tail;
       const u64 target = sender ? (base + nsteps > N ? base + nsteps - N : 0) : base + nsteps;
-      u64 seen = 0;
+      u64 seen = 0, polls = 0;
       WaitClock clk;
       while (seen < target) {
+        ++polls;
         const u64 v = ctl_acquire<kProxy>(word);
         if (v > seen) {
           seen = v;
@@ -501,6 +515,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           break;
         }
       }
+      if (cs && leader_cta) (sender ? cs->send_polls : cs->recv_polls) = polls;
     } else if (warp == 3 && leader_cta) {
       // ---------------- publisher ----------------
       // SIMPLE / zero copy: tail (sender) or head (receiver) = step + 1;
@@ -545,6 +560,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       } else if (s == nsteps) {
         ctl_store<kProxy>(basew, base + nsteps);
       }
+      if (cs && !sender) cs->t_end = globaltimer();
     }
   }
   __syncwarp();

@@ -28,7 +28,7 @@ EXPORTS = [
     "xp_ring_destroy", "xp_ring_set_lanes", "xp_ring_allreduce_virtual", "xp_ring_status", "xp_ring_reset",
     "xp_set_spin_timeout_ns", "xp_abort", "xp_status_string", "xp_last_error", "xp_version",
     "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes", "xp_send_recv_posted", "xp_fifo_enable_ce",
-    "xp_send_recv_ce", "xp_send_recv_staged",
+    "xp_send_recv_ce", "xp_send_recv_staged", "xp_fifo_stats",
 ]
 
 
@@ -43,6 +43,11 @@ class xp_channel_desc(ctypes.Structure):
                 ("nslots", ctypes.c_int), ("proto", ctypes.c_int), ("placement", ctypes.c_int),
                 ("lanes", ctypes.c_int), ("recv_lanes", ctypes.c_int), ("posted", ctypes.c_void_p),
                 ("ce", ctypes.c_void_p), ("send_ring", ctypes.c_void_p), ("recv_ring", ctypes.c_void_p)]
+
+
+class xp_channel_stats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_uint64), ("t_start_ns", ctypes.c_uint64), ("t_end_ns", ctypes.c_uint64),
+                ("send_polls", ctypes.c_uint64), ("recv_polls", ctypes.c_uint64)]
 
 
 class XpError(RuntimeError):
@@ -68,6 +73,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         "xp_fifo_enable_ce": [P],
         "xp_send_recv_ce": [P, P, P, Z, P],
         "xp_send_recv_staged": [P, P, P, P, P, Z, Z, P],
+        "xp_fifo_stats": [P, I, ctypes.POINTER(xp_channel_stats)],
         "xp_fifo_status": [P, I, ctypes.POINTER(xp_report)],
         "xp_fifo_reset": [P],
         "xp_ll_pingpong": [P, P, I, ctypes.POINTER(U64), P],
@@ -161,6 +167,12 @@ def xp_send_recv(fifo: int, src, dst, nbytes: int, stream=None) -> None:
 def xp_send_recv_zero_copy(fifo: int, src, dst, nbytes: int, stream=None) -> None:
     _check(_lib.xp_send_recv_zero_copy(fifo, _ptr(src), _ptr(dst), nbytes, _stream(stream)),
            "xp_send_recv_zero_copy")
+
+
+def xp_fifo_stats(fifo: int, channel: int) -> xp_channel_stats:
+    out = xp_channel_stats()
+    _check(_lib.xp_fifo_stats(fifo, channel, ctypes.byref(out)), "xp_fifo_stats")
+    return out
 
 
 def xp_fifo_enable_ce(fifo: int) -> None:

@@ -266,6 +266,20 @@ xp_status xp_send_recv_staged(xp_fifo* f, const void* host_src, void* host_dst, 
  * NULL.  Returns the device code (XP_OK, XP_ERR_TIMEOUT, ...). */
 xp_status xp_fifo_status(xp_fifo* f, int sync, xp_report* report);
 
+/* Per-channel record of the FIFO's last operation (after it completes):
+ * slot-steps moved, the device clock (globaltimer, ns) when the channel's
+ * sender side started and when its receiver side published its last step,
+ * and how often each side's watcher thread polled its remote counter (0 for
+ * sides and kernels without one).  Waits for the FIFO's last operation. */
+typedef struct {
+  uint64_t steps;
+  uint64_t t_start_ns;
+  uint64_t t_end_ns;
+  uint64_t send_polls;
+  uint64_t recv_polls;
+} xp_channel_stats;
+xp_status xp_fifo_stats(xp_fifo* f, int channel, xp_channel_stats* out);
+
 /* Zero the FIFO's counters, size words, ptrExchange and error state
  * (synchronous); needed after a device error. */
 xp_status xp_fifo_reset(xp_fifo* f);
@@ -342,7 +356,8 @@ xp_status xp_ring_reset(xp_ring* r);
 xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t bytes, int nchannels, int nslots,
                                size_t slot_bytes, int32_t* dev_status, xp_stream_t stream);
 
-/* Spin timeout of every device wait in later launches, in ns (default 2e9;
+/* Spin timeout of every device wait in later launches, in ns (default 2e9,
+ * or XP_SPIN_TIMEOUT_NS from the environment when the library loads;
  * 1e3 <= ns <= 6e10). */
 xp_status xp_set_spin_timeout_ns(uint64_t ns);
 

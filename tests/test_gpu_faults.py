@@ -90,3 +90,26 @@ def test_ll_flag_wait_times_out(env):
     st, _ = xp.xp_fifo_status(fifo, True)
     assert st == xp.XP_OK and np.array_equal(from_dev(out), from_dev(words))
     xp.xp_fifo_destroy(fifo)
+
+
+def test_spin_timeout_from_environment(env):
+    # XP_SPIN_TIMEOUT_NS sets the starting timeout of a fresh process: a
+    # stalled wait gives up after ~50 ms instead of the default 2 s
+    import os
+    import subprocess
+    import sys
+    code = (
+        "import time, torch\n"
+        "import collective_transport_plane_gb300.xp as xp\n"
+        "from tests.gpu_util import raw_view\n"
+        "f = xp.xp_fifo_create(1, 2, 1024)\n"
+        "raw_view(torch, xp.xp_fifo_describe(f, 0).ctl, 128, '<u8')[48] = 1000\n"
+        "torch.cuda.synchronize()\n"
+        "a = torch.ones(4096, dtype=torch.uint8, device='cuda'); b = torch.zeros_like(a)\n"
+        "t = time.time(); xp.xp_send_recv(f, a, b, 4096); st, _ = xp.xp_fifo_status(f, True)\n"
+        "print(st, time.time() - t)\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=120,
+                         env=dict(os.environ, XP_SPIN_TIMEOUT_NS="50000000"))
+    st, secs = out.stdout.split()
+    assert int(st) == 3 and float(secs) < 1.0, out.stdout + out.stderr

@@ -237,3 +237,25 @@ def test_wide_sender_lanes(env, mode):
     with pytest.raises(xp.XpError):
         xp.xp_fifo_set_recv_lanes(f, 5)           # 12 + 5 > 16
     xp.xp_fifo_destroy(f)
+
+
+@pytest.mark.parametrize("proto,place", [(0, 0), (0, 1), (1, 0)])
+def test_channel_stats(env, proto, place):
+    # per-channel records: the slot-steps the oracle's partition gives, device
+    # timestamps in order, watcher polls where a side has a watcher
+    torch, xp = env
+    C, N, S = 5, 4, 4096
+    n = 3 * 4096 * 4 + 48 if proto == 0 else 40000
+    f = xp.xp_fifo_create(C, N, S, proto, place)
+    src = to_dev(torch, workloads.uniform_bytes(n, seed=9))
+    dst = torch.zeros_like(src)
+    xp.xp_send_recv(f, src, dst, n, torch.cuda.current_stream())
+    assert xp.xp_fifo_status(f, True)[0] == xp.XP_OK
+    per_step = S if proto == 0 else S // 2       # LL lines carry 8 payload bytes per 16
+    for c, (lo, hi) in enumerate(oracle.channel_byte_ranges(n, C)):
+        st = xp.xp_fifo_stats(f, c)
+        assert st.steps == -(-(hi - lo) // per_step)
+        assert st.t_end_ns >= st.t_start_ns > 0
+        if st.steps and proto == 0 and place == 0:
+            assert st.recv_polls >= 1
+    xp.xp_fifo_destroy(f)
