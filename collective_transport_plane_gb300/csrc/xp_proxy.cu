@@ -2,17 +2,18 @@
 // (二)": p2pTransport cudaMemcopy mode, shmTransport useMemcpy mode).
 //
 // The sender kernel fills ring 0 (its own send ring) and publishes tail[0] in
-// mapped host memory.  For every channel and hop h this thread watches tail[h]
-// (hop 0) or its own progress on hop h - 1, copies newly available
-// slot-steps from ring h to ring h + 1 with cudaMemcpyAsync on a stream of
-// its own, and publishes tail[h + 1] = step + 1 once the copy's event has
-// completed.  Consecutive available steps that do not wrap around the ring
+// mapped host memory.  For every channel this thread watches tail[0], copies
+// newly available slot-steps from ring h to ring h + 1 for every hop h with
+// cudaMemcpyAsync on a stream of each hop's own (hop h + 1's copy waits on the
+// device for hop h's copy of the same steps), and publishes tail[h + 1] =
+// step + 1 once hop h's copy has completed.  Consecutive available steps that do not wrap around the ring
 // go in one copy (a run of full slots, possibly ending with a short one), so
 // every ring receives exactly the bytes of one copy per step, with far fewer
 // host calls.  (Measured on the 1 GiB, 16-channel workload: one copy per
 // step 122 GB/s, runs of up to N steps 511 GB/s; capping runs at N/2, N/4 or
 // N/8 steps was slower, 355, 219 and 117 GB/s: host calls, not overlap,
-// bound this mode.)  The receiver kernel drains the last ring.  The pump never
+// bound this mode.  Through a host-placed FIFO (two hops) runs of 1, 2, 4 or
+// N steps all gave 92-107 GB/s.)  The receiver kernel drains the last ring.  The pump never
 // decides credit: the sender only fills step s once head >= s + 1 - N, which
 // already implies that every ring's slot s mod N has been read out.
 //
@@ -72,36 +73,43 @@ struct Pump {
     failed.store(true, std::memory_order_release);
   }
 
-  // one pass over every channel and hop; true if anything moved
+  // one pass over every channel; true if anything moved
   bool poll() {
     bool moved = false;
     const int H = cfg.hops;
     const uint64_t N = (uint64_t)cfg.nslots;
     for (int c = 0; c < cfg.nchannels && !failed.load(std::memory_order_relaxed); ++c) {
-      for (int h = 0; h < H; ++h) {
-        const int q = c * H + h;
-        const uint64_t avail = h == 0 ? load_acquire(ctl(c) + kCeTailOff) : done[q - 1];
-        while (issued[q] < avail && issued[q] - done[q] < N) {
-          const uint64_t first = issued[q];
-          uint64_t lim = avail < done[q] + N ? avail : done[q] + N;
-          if (lim > first + (N - first % N)) lim = first + (N - first % N);   // no wrap within one copy
-          uint64_t end = first;
-          size_t bytes = 0;
-          while (end < lim) {
-            const int64_t sz = (int64_t)__atomic_load_n(
-                reinterpret_cast<const uint64_t*>(ctl(c) + kCeSizeOff) + end % N, __ATOMIC_RELAXED);
-            if (sz < 1 || (uint64_t)sz > cfg.slot_bytes) {
-              fail("proxy: channel " + std::to_string(c) + " step " + std::to_string(end) + " has size word " +
-                   std::to_string(sz));
-              return moved;
-            }
-            bytes += (size_t)sz;
-            ++end;
-            if ((uint64_t)sz != cfg.slot_bytes) break;   // a short step ends the run
+      const int q0 = c * H;
+      const uint64_t avail = load_acquire(ctl(c) + kCeTailOff);
+      // a batch is issued to every hop at once; hop h waits for hop h - 1's
+      // copy of the same batch on the device, so the host reacts only to
+      // completions.  At most N steps are in flight from tail[0] to the last
+      // hop's completion.
+      while (issued[q0] < avail && issued[q0] - done[q0 + H - 1] < N) {
+        const uint64_t first = issued[q0];
+        uint64_t lim = avail < done[q0 + H - 1] + N ? avail : done[q0 + H - 1] + N;
+        if (lim > first + (N - first % N)) lim = first + (N - first % N);   // no wrap within one copy
+        uint64_t end = first;
+        size_t bytes = 0;
+        while (end < lim) {
+          const int64_t sz = (int64_t)__atomic_load_n(
+              reinterpret_cast<const uint64_t*>(ctl(c) + kCeSizeOff) + end % N, __ATOMIC_RELAXED);
+          if (sz < 1 || (uint64_t)sz > cfg.slot_bytes) {
+            fail("proxy: channel " + std::to_string(c) + " step " + std::to_string(end) + " has size word " +
+                 std::to_string(sz));
+            return moved;
           }
+          bytes += (size_t)sz;
+          ++end;
+          if ((uint64_t)sz != cfg.slot_bytes) break;   // a short step ends the run
+        }
+        for (int h = 0; h < H; ++h) {
+          const int q = q0 + h;
           const size_t b = (size_t)q * N + nb_issued[q] % N;
-          cudaError_t e = cudaMemcpyAsync(slot(h + 1, c, first), slot(h, c, first), bytes, cudaMemcpyDefault,
-                                          streams[q]);
+          cudaError_t e = cudaSuccess;
+          if (h > 0) e = cudaStreamWaitEvent(streams[q], events[(size_t)(q - 1) * N + (nb_issued[q - 1] - 1) % N], 0);
+          if (e == cudaSuccess)
+            e = cudaMemcpyAsync(slot(h + 1, c, first), slot(h, c, first), bytes, cudaMemcpyDefault, streams[q]);
           if (e == cudaSuccess) e = cudaEventRecord(events[b], streams[q]);
           if (e != cudaSuccess) {
             fail(std::string("proxy: cudaMemcpyAsync: ") + cudaGetErrorString(e));
@@ -110,8 +118,11 @@ struct Pump {
           batch_end[b] = end;
           ++nb_issued[q];
           issued[q] = end;
-          moved = true;
         }
+        moved = true;
+      }
+      for (int h = 0; h < H; ++h) {
+        const int q = q0 + h;
         while (nb_done[q] < nb_issued[q]) {
           const size_t b = (size_t)q * N + nb_done[q] % N;
           const cudaError_t e = cudaEventQuery(events[b]);

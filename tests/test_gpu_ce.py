@@ -150,3 +150,37 @@ def test_ce_needs_enable_and_survives_reset(env):
         xp.xp_fifo_enable_ce(ll)
     assert e.value.status == xp.XP_ERR_INVALID
     xp.xp_fifo_destroy(ll)
+
+
+def test_pump_refuses_a_bad_size_word(env):
+    # Failure on the host side of the proxy mode, made on the host: a size
+    # word larger than a slot appears with tail[0] (written into the mapped
+    # control block while no kernel runs).  The pump stops instead of copying
+    # out of bounds, the next transfer's wait runs out, xp_fifo_status reports
+    # it with the pump's message, and a reset restarts the pump.
+    import time
+    torch, xp = env
+    f = _fifo(xp, 1, 2, 4096, 0)
+    d = xp.xp_fifo_describe(f, 0)
+    w = raw_view(torch, d.ce, 2048 // 8, "<u8")
+    w[640 // 8] = 1 << 30          # size word of slot 0
+    w[TAIL0] = 1
+    torch.cuda.synchronize()
+    time.sleep(0.2)                # the pump polls at least every 50 us
+    xp.xp_set_spin_timeout_ns(50_000_000)
+    try:
+        w[TAIL0] = 0               # leave the sender's counters consistent
+        torch.cuda.synchronize()
+        src = torch.ones(8192, dtype=torch.uint8, device="cuda")
+        dst = torch.zeros_like(src)
+        xp.xp_send_recv_ce(f, src, dst, 8192, torch.cuda.current_stream())
+        st, rep = xp.xp_fifo_status(f, True)
+        assert st == xp.XP_ERR_TIMEOUT, st
+        assert "size word 1073741824" in xp.xp_last_error()
+        xp.xp_fifo_reset(f)
+        xp.xp_set_spin_timeout_ns(2_000_000_000)
+        xp.xp_send_recv_ce(f, src, dst, 8192, torch.cuda.current_stream())
+        assert xp.xp_fifo_status(f, True)[0] == xp.XP_OK and bool((dst == 1).all())
+    finally:
+        xp.xp_set_spin_timeout_ns(2_000_000_000)
+    xp.xp_fifo_destroy(f)
