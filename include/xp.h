@@ -29,7 +29,9 @@
  *     on its stream.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); every
  *     data-moving call is asynchronous on it and launches exactly one kernel
- *     after a small cudaMemsetAsync of the operation's status block.
+ *     after a small cudaMemsetAsync of the operation's status block
+ *     (xp_send_recv_staged: one per chunk, plus its copies; xp_ll_pingpong is
+ *     synchronous).
  *   - Operations on one FIFO (or one ring) must be ordered: issue them on one
  *     stream, or synchronise between them.  Step counters live on the device
  *     and carry over from one operation to the next, so captured CUDA graphs
@@ -160,8 +162,9 @@ xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
 
 /* Receiver CTAs per channel of xp_send_recv, independently of the sender's
  * (1 <= rlanes, lanes + rlanes <= 16): the slot-step is published whole, so
- * the receiver may cut it into a different number of stripes.  Zero copy
- * always uses one receiver CTA.  SIMPLE FIFOs only. */
+ * the receiver may cut it into a different number of stripes (also for
+ * copy-mode posted and proxy transfers).  Zero copy and direct posted
+ * transfers always use one receiver CTA.  SIMPLE FIFOs only. */
 xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes);
 
 /* Channel layout (pointers stay valid until destroy). */
