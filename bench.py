@@ -229,6 +229,8 @@ def main():
     ap.add_argument("--rows", default="",
                     help="profiling only: run just these comma-separated row groups (" + ",".join(ROW_GROUPS) +
                          ") after the step, without the end-to-end and CPU legs")
+    ap.add_argument("--mode", default="simple", choices=["simple", "zero_copy", "posted_copy", "posted_direct"],
+                    help="profiling only: the transfer the timed step runs (the headline is simple)")
     ap.add_argument("--ring-mib", type=int, default=0,
                     help="profiling only: MiB per rank of the ring row instead of 256")
     args = ap.parse_args()
@@ -260,8 +262,18 @@ def main():
     xp.xp_fifo_set_lanes(fifo, args.lanes)
     xp.xp_fifo_set_recv_lanes(fifo, args.rlanes)
 
-    def step():
-        xp.xp_send_recv(fifo, src, dst, nbytes, stream)
+    if args.mode == "simple":
+        def step():
+            xp.xp_send_recv(fifo, src, dst, nbytes, stream)
+    elif args.mode == "zero_copy":
+        def step():
+            xp.xp_send_recv_zero_copy(fifo, src, dst, nbytes, stream)
+    else:
+        direct = args.mode == "posted_direct"
+
+        def step():
+            xp.xp_send_recv_posted(fifo, src, dst, nbytes, direct, stream)
+    per_byte = 2 if args.mode in ("zero_copy", "posted_direct") else 4
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -289,7 +301,7 @@ def main():
     ms_step = total_ms / args.steps
     value = whole_job_gbs(world, nbytes, args.steps, total_ms)
     avg_launch_ms = statistics.mean(per)
-    achieved = 4 * nbytes / (avg_launch_ms * 1e-3) / 1e9
+    achieved = per_byte * nbytes / (avg_launch_ms * 1e-3) / 1e9
 
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -302,14 +314,17 @@ def main():
                    "l2": "inputs (1 GiB) larger than L2; the 64 MiB FIFO itself is L2-resident by design"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
+                     "frac": achieved / hbm_peak, "traffic": profiled_traffic() if args.mode == "simple" else None,
                      "peak_kind": f"{peak_kind} HBM copy (burst)",
-                     "accounting": "4 bytes per payload byte: src read, slot write, slot read, dst write"},
+                     "accounting": "4 bytes per payload byte: src read, slot write, slot read, dst write"
+                                   if per_byte == 4 else "2 bytes per payload byte: src read, dst write"},
         "clocks": clk,
     }
 
     if args.mib:
         out["config"]["workload"] += f" (profiling case: first {args.mib} MiB)"
+    if args.mode != "simple":
+        out["config"]["workload"] += f" (profiling case: {args.mode} transfer)"
     if rank == 0 and args.rows:
         out["rows"] = rows(torch, xp, hbm_peak, set(args.rows.split(",")), args.ring_mib)
     elif rank == 0 and not args.no_rows:
