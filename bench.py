@@ -220,8 +220,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--lanes", type=int, default=6, help="sender CTAs per channel")
-    ap.add_argument("--rlanes", type=int, default=7, help="receiver CTAs per channel")
+    ap.add_argument("--lanes", type=int, default=10, help="sender CTAs per channel")
+    ap.add_argument("--rlanes", type=int, default=8, help="receiver CTAs per channel")
     ap.add_argument("--no-rows", action="store_true", help="time the step only")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--mib", type=int, default=0,
@@ -426,7 +426,7 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         # staging slots (4 bytes of HBM traffic per payload byte) and direct
         # mode into dst (2 bytes per payload byte)
         posted = {}
-        for direct, lanes, rl in ((False, 6, 7), (True, 12, None)):
+        for direct, lanes, rl in ((False, 10, 8), (True, 8, None)):
             f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
             xp.xp_fifo_set_lanes(f, lanes)
             if rl:

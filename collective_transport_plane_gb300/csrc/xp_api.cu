@@ -245,25 +245,33 @@ xp_status launch(const void* kernel, int grid, int block, int csize, void* param
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// CTAs of the bulk-copy ring kernel resident on this GPU at once
-int ring_tma_resident() {
-  static std::atomic<int> cached{-1};
-  int v = cached.load();
-  if (v >= 0) return v;
+// CTAs of `kernel` (block threads, smem bytes of dynamic shared memory)
+// resident on this GPU at once; 0 if unknown.
+std::map<const void*, int> g_resident;
+int resident_ctas(const void* kernel, int block, int smem) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_resident.find(kernel);
+    if (it != g_resident.end()) return it->second;
+  }
   int per_sm = 0, dev = 0, sms = 0;
-  if (cudaFuncSetAttribute(xp::ring_tma_kernel_ptr(XP_F32), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           xp::ring_tma_smem()) != cudaSuccess ||
-      cudaFuncSetAttribute(xp::ring_tma_kernel_ptr(XP_I32), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           xp::ring_tma_smem()) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, xp::ring_tma_kernel_ptr(XP_F32), xp::ring_tma_threads(),
-                                                    (size_t)xp::ring_tma_smem()) != cudaSuccess ||
+  if ((smem > 48 * 1024 &&
+       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, (size_t)smem) != cudaSuccess ||
       cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     (void)cudaGetLastError();
-    return 0;   // unknown: use clusters
+    return 0;
   }
-  v = per_sm * sms;
-  cached.store(v);
-  return v;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_resident[kernel] = per_sm * sms;
+  return per_sm * sms;
+}
+
+// CTAs of the bulk-copy ring kernel resident on this GPU at once
+int ring_tma_resident() {
+  const int a = resident_ctas(xp::ring_tma_kernel_ptr(XP_F32), xp::ring_tma_threads(), xp::ring_tma_smem());
+  const int b = resident_ctas(xp::ring_tma_kernel_ptr(XP_I32), xp::ring_tma_threads(), xp::ring_tma_smem());
+  return a < b ? a : b;
 }
 
 // Marks the object's last operation on `st`.  Inside a stream capture the
@@ -301,6 +309,7 @@ struct xp_fifo {
   char* ctl = nullptr;     // device view
   char* slots = nullptr;   // device view
   char* pctl = nullptr;    // device view: posted-FIFO blocks
+  unsigned long long* arr = nullptr;   // device: lane arrival counters (always HBM)
   xp::ChanStats* stats = nullptr;   // device: one record per channel
   size_t ctl_region = 0;
   size_t pctl_region = 0;
@@ -392,8 +401,11 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
     return s;
   }
   if (cudaMalloc(reinterpret_cast<void**>(&f->stats), (size_t)nchannels * sizeof(xp::ChanStats)) != cudaSuccess ||
-      cudaMemset(f->stats, 0, (size_t)nchannels * sizeof(xp::ChanStats)) != cudaSuccess) {
+      cudaMemset(f->stats, 0, (size_t)nchannels * sizeof(xp::ChanStats)) != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&f->arr), (size_t)nchannels * xp::kArrBytes) != cudaSuccess ||
+      cudaMemset(f->arr, 0, (size_t)nchannels * xp::kArrBytes) != cudaSuccess) {
     if (f->stats) cudaFree(f->stats);
+    if (f->arr) cudaFree(f->arr);
     common_free(f->cm);
     mem_free(f->mem);
     delete f;
@@ -417,6 +429,7 @@ xp_status xp_fifo_destroy(xp_fifo* f) {
   common_free(f->cm);
   mem_free(f->mem);
   if (f->stats) cudaFree(f->stats);
+  if (f->arr) cudaFree(f->arr);
   mem_free(f->ce_mem);
   mem_free(f->ring_mem);
   delete f;
@@ -474,17 +487,16 @@ xp_status xp_fifo_enable_ce(xp_fifo* f) {
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
-  if (lanes < 1 || lanes > xp::kMaxCluster - 1) return fail(XP_ERR_INVALID, "lanes %d not in [1, 15]", lanes);
+  if (lanes < 1 || lanes > xp::kMaxLanes) return fail(XP_ERR_INVALID, "lanes %d not in [1, 32]", lanes);
   f->lanes = lanes;
-  f->rlanes = lanes <= xp::kMaxCluster / 2 ? lanes : xp::kMaxCluster - lanes;
+  f->rlanes = lanes <= xp::kMaxCluster / 2 ? lanes : (lanes < xp::kMaxCluster ? xp::kMaxCluster - lanes : 1);
   return XP_OK;
 }
 
 xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
-  if (rlanes < 1 || f->lanes + rlanes > xp::kMaxCluster)
-    return fail(XP_ERR_INVALID, "receiver lanes %d: need 1 <= rlanes and lanes + rlanes <= 16", rlanes);
+  if (rlanes < 1 || rlanes > xp::kMaxLanes) return fail(XP_ERR_INVALID, "receiver lanes %d not in [1, 32]", rlanes);
   f->rlanes = rlanes;
   return XP_OK;
 }
@@ -528,6 +540,7 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   xp::P2pParams p = {};
   p.ctl = f->ctl;
+  p.arr = f->arr;
   p.stats = f->stats;
   p.pctl = f->pctl;
   p.ce = f->ce_mem.dev;
@@ -556,8 +569,6 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     p.lanes = f->lanes;
     p.rlanes = (zero_copy || mode == kOpPostedDirect) ? 1 : f->rlanes;
     csize = p.lanes + p.rlanes;
-    if (csize > xp::kMaxCluster)
-      return fail(XP_ERR_INVALID, "%d sender + %d receiver CTAs per channel exceed a cluster of 16", p.lanes, p.rlanes);
     if (f->place == XP_PLACE_DEVICE || mode == kOpProxy) {
       // HBM FIFO (or the proxy mode's device rings): bulk copies through shared memory
       kernel = xp::p2p_tma_kernel_ptr(mode);
@@ -570,8 +581,18 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     }
   }
   p.csize = csize;
+  // The bulk-copy kernel needs the sender and receiver CTAs of a channel
+  // resident together: a cooperative grid when all of it fits at once (no
+  // cluster placement limits), else one cluster per channel.  The other
+  // kernels always use clusters.
+  int launch_csize = csize;
+  if (kernel == xp::p2p_tma_kernel_ptr(mode) && f->C * csize <= resident_ctas(kernel, block, smem))
+    launch_csize = 0;
+  if (launch_csize > xp::kMaxCluster)
+    return fail(XP_ERR_INVALID, "%d channels x %d CTAs neither fit on the GPU at once nor form clusters of at most 16",
+                f->C, csize);
   XP_CUDA(cudaMemsetAsync(f->cm.status, 0, xp::kStatusClearBytes, st));
-  if ((s = launch(kernel, f->C * csize, block, csize, &p, st, smem)) != XP_OK) return s;
+  if ((s = launch(kernel, f->C * csize, block, launch_csize, &p, st, smem)) != XP_OK) return s;
   if (mode == kOpProxy) xp::pump_kick(f->pump);
   return record_done(f->cm, st);
 }
@@ -659,6 +680,7 @@ xp_status xp_fifo_reset(xp_fifo* f) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (f->cm.used) XP_CUDA(cudaEventSynchronize(f->cm.done));
   XP_CUDA(cudaMemset(f->cm.status, 0, sizeof(DevStatus)));
+  XP_CUDA(cudaMemset(f->arr, 0, (size_t)f->C * xp::kArrBytes));
   if (f->pump) {
     // restart the pump on zeroed proxy counters
     xp::pump_stop(f->pump);

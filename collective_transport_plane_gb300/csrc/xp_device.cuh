@@ -28,6 +28,12 @@ __device__ __forceinline__ void st_release(u64* p, u64 v) {
 __device__ __forceinline__ void st_relaxed(u64* p, u64 v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void red_add_release(u64* p, u64 v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_add_relaxed(u64* p, u64 v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 // .sys scope: words shared with a host thread (the proxy mode's pump)
 __device__ __forceinline__ u64 ld_acquire_sys(const u64* p) {
   u64 v;

@@ -12,6 +12,7 @@ constexpr int kMaxSlots = 64;
 constexpr int kMaxChannels = 64;
 constexpr int kMaxRanks = 16;
 constexpr int kMaxCluster = 16;
+constexpr int kMaxLanes = 32;     // CTAs per side of a channel (bulk-copy channel kernel)
 
 // Per-channel control block: every word the two sides write sits on its own
 // 128-byte line, so the producer's tail stores and the consumer's head stores
@@ -44,6 +45,11 @@ constexpr int kCeTailOff = 0;          // tail[h] at kCeTailOff + 128 h
 constexpr int kCeHeadOff = 384;
 constexpr int kCeBaseOff = 512;
 constexpr int kCeSizeOff = 640;        // kMaxSlots int64 size words
+
+// Per-channel arrival counters of the bulk-copy channel kernel's lanes: one
+// uint64 per slot for the sender side, then one per slot for the receiver
+// side; zero between operations.
+constexpr int kArrBytes = 16 * kMaxSlots;
 
 constexpr int kCopyWarps = 16;                  // data-moving warps per CTA
 constexpr int kP2pThreads = 32 * (kCopyWarps + 1);   // + 1 publisher warp
@@ -84,6 +90,7 @@ static_assert(sizeof(ChanStats) == 64, "stats record layout");
 
 struct P2pParams {
   char* ctl;                      // nchannels control blocks
+  unsigned long long* arr;        // nchannels arrival blocks (bulk-copy channel kernel)
   ChanStats* stats;               // nchannels records, or nullptr
   char* pctl;                     // nchannels posted-FIFO blocks (posted transfers)
   char* ce;                       // nchannels proxy-mode blocks (mapped host memory)

@@ -28,7 +28,8 @@ constexpr int kNoallocMaxChannels = 16;
 constexpr size_t kNoallocSlotBytes = 8u << 20;   // every channel's slots together
 constexpr size_t kNoallocStatusOff = 0;
 constexpr size_t kNoallocCtlOff = 256;
-constexpr size_t kNoallocSlotsOff = kNoallocCtlOff + (size_t)kNoallocMaxChannels * xp::kCtlBytes;
+constexpr size_t kNoallocArrOff = kNoallocCtlOff + (size_t)kNoallocMaxChannels * xp::kCtlBytes;
+constexpr size_t kNoallocSlotsOff = kNoallocArrOff + (size_t)kNoallocMaxChannels * xp::kArrBytes;
 constexpr size_t kNoallocBytes = kNoallocSlotsOff + kNoallocSlotBytes;
 constexpr unsigned long long kNoallocTimeoutNs = 2000000000ull;
 
@@ -94,12 +95,13 @@ extern "C" xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t byt
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   xp::DevStatus* status = reinterpret_cast<xp::DevStatus*>(base + kNoallocStatusOff);
-  // counters, ptrExchange, step base and status start at zero on every call
-  if ((e = cudaMemsetAsync(base, 0, kNoallocCtlOff + (size_t)nchannels * xp::kCtlBytes, st)) != cudaSuccess)
-    return cuda_failed("cudaMemsetAsync", e);
+  // status, counters, ptrExchange, step base and lane arrival counters start
+  // at zero on every call
+  if ((e = cudaMemsetAsync(base, 0, kNoallocSlotsOff, st)) != cudaSuccess) return cuda_failed("cudaMemsetAsync", e);
 
   xp::P2pParams p = {};
   p.ctl = reinterpret_cast<char*>(base + kNoallocCtlOff);
+  p.arr = reinterpret_cast<unsigned long long*>(base + kNoallocArrOff);
   p.slots = reinterpret_cast<char*>(base + kNoallocSlotsOff);
   p.ch_stride = ch_stride;
   p.src = static_cast<const char*>(src);

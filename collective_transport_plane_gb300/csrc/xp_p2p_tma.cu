@@ -2,9 +2,13 @@
 // shared memory: SIMPLE, zero copy, receiver-driven credit (copy and direct
 // modes) and the proxy (copy-engine) mode, one template instance each.
 //
-// Cluster layout as in the vector kernels (xp_p2p.cu): per channel, CTAs
-// [0, G) send and [G, G + GR) receive (zero copy and direct posts: CTA G
-// receives).  Each CTA moves one contiguous stripe of every slot-step
+// Per channel, CTAs [0, G) send and [G, G + GR) receive (zero copy and direct
+// posts: CTA G receives), consecutive in the grid.  The lanes of a side share
+// the channel's counters through per-slot arrival counters in global memory,
+// so no thread-block cluster is needed: the host launches the grid
+// cooperatively when all of it is resident at once (sender and receiver CTAs
+// that wait on each other must run together), else as one cluster per
+// channel.  Each CTA moves one contiguous stripe of every slot-step
 // ("lane") through a ring of kTmaStages shared-memory stages:
 //   sender    - one mover thread issues bulk loads from src up to kLookSend
 //               entries ahead (they need nothing) and bulk stores into the
@@ -18,7 +22,7 @@
 //               mirrors it into shared memory, so no copying thread stalls on
 //               a global-memory round trip;
 //   publisher - in the side's leader CTA only: waits until all lanes have
-//               signalled a slot-step on its mbarrier and publishes the one
+//               signalled a slot-step on its arrival counter and publishes the one
 //               channel-wide counter (tail = step + 1 on the sender side,
 //               head = step + 1 on the receiver side; posted modes: the
 //               completion, or the next post).
@@ -27,7 +31,7 @@
 // store pipeline never drains at a step boundary, and before it blocks on
 // credit it reports whatever is pending (a FIFO of one slot would otherwise
 // wait on itself).  It reports through shared memory to a signaler thread,
-// which does the cluster-scope release arrive: a release waits for the
+// which does the release add on the arrival counter: a release waits for the
 // issuing thread's in-flight memory traffic, and the mover always has some.
 // A receiver stripe is signalled as soon as its bulk loads from the slot have
 // landed in shared memory.  Slot traffic is marked evict_last in L2 and
@@ -149,7 +153,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   constexpr bool kToUser = kZeroCopy || kDirect;   // the sender writes dst itself
   constexpr bool kProxy = kMode == kModeProxy;
   extern __shared__ __align__(128) char stage_mem[];
-  __shared__ __align__(8) u64 bars[kMaxSlots];
   __shared__ __align__(8) u64 full[kTmaStages];
   __shared__ __align__(8) u64 empty[kTmaStages];   // receiver: stage free again
   __shared__ u64 s_base;
@@ -161,7 +164,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const unsigned crank = cluster_ctarank();
+  const unsigned crank = blockIdx.x % p.csize;   // CTA within its channel
   const int ch = blockIdx.x / p.csize;
   const int G = p.lanes;                        // sender lanes
   const int GR = kToUser ? 1 : p.rlanes;        // receiver lanes
@@ -222,11 +225,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       mbar_init(smem_addr(&full[k]), 1);
       mbar_init(smem_addr(&empty[k]), 1);
     }
-    if (leader_cta)
-      for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), (uint32_t)GS);
     mbar_init_fence();
   }
-  cluster_sync_all();
+  __syncthreads();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
   ChanStats* cs = p.stats ? p.stats + ch : nullptr;
@@ -239,7 +240,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
     if (!run) cs->t_end = t;
   }
   const uint32_t sm0 = smem_addr(stage_mem);
-  const uint32_t bar0 = map_to_rank(smem_addr(&bars[0]), leader);
+  // Per-slot arrival counters of this side: each lane adds 1 when it is done
+  // with its stripe of a slot-step, the side's publisher waits for all GS
+  // lanes and takes them back off (so the counters are zero between
+  // operations).
+  u64* arrivals = p.arr + (u64)ch * (kArrBytes / 8) + (sender ? 0 : kMaxSlots);
   const u64 pol_slot = policy_evict_last();     // FIFO slots: reused every N steps
   // src / dst are read or written once: evict first where FIFO slots share the
   // L2 with them, normal priority where nothing else is kept (zero copy and
@@ -430,14 +435,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         mbar_wait_cta(smem_addr(&full[i % K]), (uint32_t)((i / K) & 1), w);
     } else if (warp == 1 && sender) {
       // ---------------- sender signaler ----------------
-      // Turns each "stores of step s complete" from the mover into the
-      // cluster-scope release arrive on the slot's barrier in the leader
-      // CTA.  A release waits for the issuing thread's own memory traffic;
-      // this thread has none in flight, the mover always has.
+      // Turns each "stores of step s complete" from the mover into a release
+      // add on the slot's arrival counter.  A release waits for the issuing
+      // thread's own memory traffic; this thread has none in flight, the
+      // mover always has.
       u64 done = 0;
       for (u64 s = 0; s < nsteps; ++s) {
         if (!wait_mirror(&s_done, s + 1, done, w, XP_WAIT_SLOT_BARRIER)) break;
-        mbar_arrive_cluster(bar0 + 8u * (uint32_t)((base + s) % N));
+        red_add_release(arrivals + (base + s) % N, 1);
       }
     } else if (warp == 1 && !sender) {
       // ---------------- receiver storer ----------------
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           // The slot's bytes for this stripe are in shared memory (its ragged
           // bytes were copied before the first load of the step): the reads
           // are complete, so the signal carries no ordering.
-          if (e + 1 == st.nent) mbar_arrive_cluster_relaxed(bar0 + 8u * (uint32_t)((base + s) % N));
+          if (e + 1 == st.nent) red_add_relaxed(arrivals + (base + s) % N, 1);
           const uint32_t nb = entry_bytes(st, e);
           if (nb) bulk_store(p.dst + lo + s * S + st.b0 + e * kTmaChunk, sm0 + k * kTmaChunk, nb, pol_user);
           bulk_commit();
@@ -533,7 +538,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       }
       for (; s < nsteps; ++s) {
         const u64 step = base + s;
-        if (!mbar_wait(smem_addr(&bars[step % N]), (uint32_t)((s / N) & 1), w, XP_WAIT_SLOT_BARRIER, step)) break;
+        {
+          u64 c = 0;
+          if (!wait_geq(arrivals + step % N, (u64)GS, c, w, XP_WAIT_SLOT_BARRIER)) break;
+          red_add_relaxed(arrivals + step % N, 0ull - (u64)GS);
+        }
         if (kPosted) {
           if (sender) {
             st_relaxed(cq + 2 * (step % N), step_size(s));
@@ -567,7 +576,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
     }
   }
   __syncwarp();
-  cluster_sync_all();
 }
 
 template __global__ void p2p_tma_kernel<kModeSimple>(const P2pParams);

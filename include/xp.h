@@ -341,7 +341,7 @@ xp_status xp_ring_reset(xp_ring* r);
  * re-enter the allocator) or under a hard device-memory budget.  The caller
  * passes src and dst as for xp_send_recv; the FIFO (control blocks, slots,
  * status) lives in one static device array of this library, 8 MiB of slots
- * plus 16.25 KiB, that every GPU which loads the library keeps reserved until
+ * plus 32.25 KiB, that every GPU which loads the library keeps reserved until
  * the process exits.  Limits: 1 <= nchannels <= 16, 1 <= nslots <= 64,
  * slot_bytes a non-zero multiple of 16, and nchannels x
  * round_up(nslots x slot_bytes, 4096) <= 8 MiB; larger FIFOs are refused with

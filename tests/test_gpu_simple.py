@@ -235,7 +235,34 @@ def test_wide_sender_lanes(env, mode):
     assert np.array_equal(from_dev(dst), want)
     assert xp.xp_fifo_describe(f, 0).recv_lanes == 4
     with pytest.raises(xp.XpError):
-        xp.xp_fifo_set_recv_lanes(f, 5)           # 12 + 5 > 16
+        xp.xp_fifo_set_recv_lanes(f, 33)
+    xp.xp_fifo_destroy(f)
+
+
+def test_lanes_beyond_a_cluster_and_the_cluster_fallback(env):
+    # 12 + 10 CTAs per channel: more than a cluster holds, fine while the whole
+    # grid is resident (cooperative launch); 64 channels of 4 + 4 CTAs do not
+    # fit at once and run as clusters; 64 x (12 + 10) fits neither way
+    torch, xp = env
+    for nchan, lanes, rl in ((5, 12, 10), (64, 4, 4)):
+        src_np = workloads.uniform_bytes((5 << 20) + 77, seed=nchan)
+        want = oracle.simple_transfer(src_np, nchan, 4, 16384, seed=3)[0]
+        f = xp.xp_fifo_create(nchan, 4, 16384)
+        xp.xp_fifo_set_lanes(f, lanes)
+        xp.xp_fifo_set_recv_lanes(f, rl)
+        src = to_dev(torch, src_np)
+        dst = torch.zeros_like(src)
+        xp.xp_send_recv(f, src, dst, src_np.nbytes, torch.cuda.current_stream())
+        st, rep = xp.xp_fifo_status(f, True)
+        assert st == xp.XP_OK, (nchan, st, rep.where)
+        assert np.array_equal(from_dev(dst), want)
+        xp.xp_fifo_destroy(f)
+    f = xp.xp_fifo_create(64, 4, 16384)
+    xp.xp_fifo_set_lanes(f, 12)
+    xp.xp_fifo_set_recv_lanes(f, 10)
+    with pytest.raises(xp.XpError) as e:
+        xp.xp_send_recv(f, src, dst, 4096, torch.cuda.current_stream())
+    assert e.value.status == xp.XP_ERR_INVALID
     xp.xp_fifo_destroy(f)
 
 
