@@ -305,6 +305,7 @@ struct xp_fifo {
   xp_placement place = XP_PLACE_DEVICE;
   int lanes = 1;           // sender CTAs per channel
   int rlanes = 1;          // receiver CTAs per channel
+  int discard = 1;         // receivers drop the slot lines they read from L2
   Mem mem;
   char* ctl = nullptr;     // device view
   char* slots = nullptr;   // device view
@@ -501,6 +502,12 @@ xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes) {
   return XP_OK;
 }
 
+xp_status xp_fifo_set_discard(xp_fifo* f, int on) {
+  if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
+  f->discard = on ? 1 : 0;
+  return XP_OK;
+}
+
 xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out) {
   if (!f || !out) return fail(XP_ERR_INVALID, "NULL argument");
   if (channel < 0 || channel >= f->C) return fail(XP_ERR_INVALID, "channel %d out of range", channel);
@@ -547,6 +554,7 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   p.send_ring = f->send_ring;
   p.recv_ring = f->recv_ring;
   p.hops = f->hops;
+  p.discard = f->discard;
   p.slots = f->slots;
   p.ch_stride = f->ch_stride;
   p.src = static_cast<const char*>(src);

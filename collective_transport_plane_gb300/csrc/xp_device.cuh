@@ -28,6 +28,11 @@ __device__ __forceinline__ void st_release(u64* p, u64 v) {
 __device__ __forceinline__ void st_relaxed(u64* p, u64 v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+// Drop the 128-byte line at p (128-byte aligned) from L2 without writing it
+// back; its contents become undefined.
+__device__ __forceinline__ void discard_l2(void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ void red_add_release(u64* p, u64 v) {
   asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }

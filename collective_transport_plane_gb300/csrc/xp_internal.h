@@ -97,6 +97,7 @@ struct P2pParams {
   char* send_ring;                // proxy mode: the sender's own slots, same geometry as `slots`
   char* recv_ring;                // proxy mode: the slots the receiver drains
   int hops;                       // proxy mode: host-driven copies per slot-step (1 or 2)
+  int discard;                    // receivers drop read slot lines from L2 (bulk-copy kernel)
   char* slots;                    // channel c's slot k at slots + c*ch_stride + k*slot_bytes
   unsigned long long ch_stride;
   const char* src;

@@ -101,6 +101,7 @@ extern "C" xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t byt
 
   xp::P2pParams p = {};
   p.ctl = reinterpret_cast<char*>(base + kNoallocCtlOff);
+  p.discard = 1;
   p.arr = reinterpret_cast<unsigned long long*>(base + kNoallocArrOff);
   p.slots = reinterpret_cast<char*>(base + kNoallocSlotsOff);
   p.ch_stride = ch_stride;

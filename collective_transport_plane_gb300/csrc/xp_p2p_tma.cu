@@ -52,7 +52,15 @@ constexpr uint32_t kTmaChunk = 16384;
 constexpr int kLookSend = 4;
 constexpr int kLookZeroCopy = 3;
 constexpr int kRecvStoresInFlight = 3;   // receiver: dst stores still reading their stage
-constexpr int kTmaThreads = 128;
+// Receivers that read FIFO slots invalidate in L2, with discard.global.L2,
+// the 128-byte lines of their stripe that they have read, before returning
+// credit: the slot's dirty bytes are dead once read, and without this they are
+// written back to DRAM whenever L2 evicts them before the slot is refilled.
+// A fifth warp does it, so the copy pipeline never waits for it.  The
+// operation's `discard` flag turns it off (the slots then keep the last bytes
+// that passed through them).
+constexpr bool kDiscard = true;
+constexpr int kTmaThreads = kDiscard ? 160 : 128;
 constexpr int kTmaSmem = kTmaStages * (int)kTmaChunk;
 constexpr int kDefer = 4;
 static_assert(kLookSend < kTmaStages && kLookZeroCopy < kTmaStages && kRecvStoresInFlight < kTmaStages,
@@ -158,6 +166,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   __shared__ u64 s_base;
   __shared__ u64 s_mirror;   // latest head / post (sender) or tail / completion (receiver) seen by the watcher
   __shared__ u64 s_done;     // sender: steps [0, s_done) have their bulk stores complete
+  __shared__ u64 s_read;     // receiver: steps [0, s_read) have their slot stripe in shared memory
   __shared__ u64 s_addr[kPosted ? kMaxSlots : 1];   // posted sender: address and size of each slot's post
   __shared__ u64 s_cap[kPosted ? kMaxSlots : 1];
   __shared__ int s_stop;
@@ -221,6 +230,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
     }
     s_mirror = 0;
     s_done = 0;
+    s_read = 0;
     for (int k = 0; k < kTmaStages; ++k) {
       mbar_init(smem_addr(&full[k]), 1);
       mbar_init(smem_addr(&empty[k]), 1);
@@ -230,6 +240,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   __syncthreads();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
+  const bool discard = kDiscard && !kToUser && p.discard != 0;
   ChanStats* cs = p.stats ? p.stats + ch : nullptr;
   if (cs && sender && leader_cta && threadIdx.x == 0) {
     const u64 t = globaltimer();
@@ -460,7 +471,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           // The slot's bytes for this stripe are in shared memory (its ragged
           // bytes were copied before the first load of the step): the reads
           // are complete, so the signal carries no ordering.
-          if (e + 1 == st.nent) red_add_relaxed(arrivals + (base + s) % N, 1);
+          if (e + 1 == st.nent) {
+            if (discard)
+              st_release_cta_shared(&s_read, s + 1);   // the discarder returns the credit
+            else
+              red_add_relaxed(arrivals + (base + s) % N, 1);
+          }
           const uint32_t nb = entry_bytes(st, e);
           if (nb) bulk_store(p.dst + lo + s * S + st.b0 + e * kTmaChunk, sm0 + k * kTmaChunk, nb, pol_user);
           bulk_commit();
@@ -573,6 +589,27 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         ctl_store<kProxy>(basew, base + nsteps);
       }
       if (cs && !sender) cs->t_end = globaltimer();
+    }
+  }
+  if (discard && run && !sender && warp == 4) {
+    // ---------------- discarder ----------------
+    // once the storer has seen a step's stripe land in shared memory, drop
+    // the 128-byte lines lying wholly inside the stripe from L2 (lines shared
+    // with a neighbouring lane's stripe stay), then signal the slot consumed
+    Entries en;
+    en.init(len, S, (u64)GS, (u64)lane_id);
+    u64 seen = 0;
+    for (u64 s = 0; s < nsteps; ++s) {
+      int ok = 1;
+      if (lane == 0) ok = wait_mirror(&s_read, s + 1, seen, w, XP_WAIT_SLOT_BARRIER) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const Stripe& st = en.stripe(s);
+      const u64 from = reinterpret_cast<u64>(slots_recv + ((base + s) % N) * S);
+      const u64 l0 = (from + st.b0 + 127) & ~127ull;
+      const u64 l1 = (from + st.b0 + st.fb + st.rag) & ~127ull;
+      for (u64 x = l0 + 128ull * lane; x < l1; x += 128ull * 32) discard_l2(reinterpret_cast<void*>(x));
+      __syncwarp();
+      if (lane == 0) red_add_release(arrivals + (base + s) % N, 1);
     }
   }
   __syncwarp();

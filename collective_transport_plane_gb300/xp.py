@@ -28,7 +28,7 @@ EXPORTS = [
     "xp_ring_destroy", "xp_ring_set_lanes", "xp_ring_allreduce_virtual", "xp_ring_status", "xp_ring_reset",
     "xp_set_spin_timeout_ns", "xp_abort", "xp_status_string", "xp_last_error", "xp_version",
     "xp_send_recv_noalloc", "xp_fifo_set_recv_lanes", "xp_send_recv_posted", "xp_fifo_enable_ce",
-    "xp_send_recv_ce", "xp_send_recv_staged", "xp_fifo_stats",
+    "xp_send_recv_ce", "xp_send_recv_staged", "xp_fifo_stats", "xp_fifo_set_discard",
 ]
 
 
@@ -74,6 +74,7 @@ def load(path: str = _LIB_PATH) -> ctypes.CDLL:
         "xp_send_recv_ce": [P, P, P, Z, P],
         "xp_send_recv_staged": [P, P, P, P, P, Z, Z, P],
         "xp_fifo_stats": [P, I, ctypes.POINTER(xp_channel_stats)],
+        "xp_fifo_set_discard": [P, I],
         "xp_fifo_status": [P, I, ctypes.POINTER(xp_report)],
         "xp_fifo_reset": [P],
         "xp_ll_pingpong": [P, P, I, ctypes.POINTER(U64), P],
@@ -173,6 +174,10 @@ def xp_fifo_stats(fifo: int, channel: int) -> xp_channel_stats:
     out = xp_channel_stats()
     _check(_lib.xp_fifo_stats(fifo, channel, ctypes.byref(out)), "xp_fifo_stats")
     return out
+
+
+def xp_fifo_set_discard(fifo: int, on: bool) -> None:
+    _check(_lib.xp_fifo_set_discard(fifo, 1 if on else 0), "xp_fifo_set_discard")
 
 
 def xp_fifo_enable_ce(fifo: int) -> None:

@@ -167,6 +167,16 @@ xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
  * transfers always use one receiver CTA.  SIMPLE FIFOs only. */
 xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes);
 
+/* Whether receivers that read FIFO slots in HBM drop each 128-byte line of
+ * their stripe from L2 (discard.global.L2) once they have read it, before
+ * returning credit (on != 0, the default) — the data is dead, and this saves
+ * writing it back to DRAM — or leave it (on == 0).  With it on, the slots'
+ * bytes after a transfer are undefined; with it off they hold the last
+ * slot-steps that passed through, as in the pages' protocol.  Applies to
+ * xp_send_recv, copy-mode xp_send_recv_posted and xp_send_recv_ce on HBM
+ * FIFOs; takes effect at the next operation. */
+xp_status xp_fifo_set_discard(xp_fifo* f, int on);
+
 /* Channel layout (pointers stay valid until destroy). */
 xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out);
 

@@ -26,7 +26,7 @@ def xp():
 
 def test_every_declared_symbol_is_exported(xp):
     names = _declared()
-    assert len(names) == 27, names
+    assert len(names) == 28, names
     out = subprocess.run(["nm", "-D", "--defined-only", xp.library_path()], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (xp_[a-z0-9_]+)", out))
     assert set(names) <= exported

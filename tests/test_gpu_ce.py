@@ -25,8 +25,10 @@ def env():
     return torch, xp
 
 
-def _fifo(xp, nchan, nslots, slot, place, lanes=1, rlanes=None):
+def _fifo(xp, nchan, nslots, slot, place, lanes=1, rlanes=None, discard=False):
+    # ring contents are checked against the oracle's: no discard unless asked
     f = xp.xp_fifo_create(nchan, nslots, slot, xp.XP_PROTO_SIMPLE, place)
+    xp.xp_fifo_set_discard(f, discard)
     xp.xp_fifo_set_lanes(f, lanes)
     if rlanes is not None:
         xp.xp_fifo_set_recv_lanes(f, rlanes)

@@ -25,7 +25,9 @@ def env():
 
 
 def _fifo(xp, nchan, nslots, slot, lanes=1, rlanes=None):
+    # slots keep their last bytes (checked against the oracle's): no discard
     f = xp.xp_fifo_create(nchan, nslots, slot, xp.XP_PROTO_SIMPLE, xp.XP_PLACE_DEVICE)
+    xp.xp_fifo_set_discard(f, False)
     xp.xp_fifo_set_lanes(f, lanes)
     if rlanes is not None:
         xp.xp_fifo_set_recv_lanes(f, rlanes)
@@ -172,3 +174,20 @@ def test_posted_refused_after_error_and_bad_fifos(env):
             xp.xp_send_recv_posted(f, src, dst, 64, False, torch.cuda.current_stream())
         assert e.value.status == xp.XP_ERR_INVALID
         xp.xp_fifo_destroy(f)
+
+
+@pytest.mark.parametrize("lanes,rlanes", [(1, 1), (3, 5)])
+def test_posted_copy_with_discard(env, lanes, rlanes):
+    # with the receivers dropping read slot lines from L2, the delivered bytes,
+    # posts and completions still equal the oracle's (the slots' final bytes
+    # are undefined and not compared)
+    torch, xp = env
+    n, nchan, nslots, slot = 1000003, 5, 3, 65536 + 48
+    src_np = workloads.uniform_bytes(n, seed=91)
+    want, chans, _ = oracle.posted_transfer(src_np, nchan, nslots, slot, seed=2)
+    fifo = _fifo(xp, nchan, nslots, slot, lanes, rlanes)
+    xp.xp_fifo_set_discard(fifo, True)
+    _, dst, _ = _posted(torch, xp, fifo, src_np, False)
+    assert np.array_equal(from_dev(dst), want)
+    _check_state(torch, xp, fifo, chans, nslots, slot, dst.data_ptr(), False, [0] * nchan)
+    xp.xp_fifo_destroy(fifo)

@@ -286,3 +286,28 @@ def test_channel_stats(env, proto, place):
         if st.steps and proto == 0 and place == 0:
             assert st.recv_polls >= 1
     xp.xp_fifo_destroy(f)
+
+
+@pytest.mark.parametrize("discard", [True, False])
+def test_slot_contents_only_without_discard(env, discard):
+    # slot sizes that are not multiples of 128 bytes put line boundaries inside
+    # stripes and across slots; delivered bytes are exact either way, and with
+    # discard off the slots keep the oracle's last slot-steps
+    torch, xp = env
+    n, nchan, nslots, slot = 777777, 3, 4, 4096 + 80
+    src_np = workloads.uniform_bytes(n, seed=17)
+    want, fifos, _ = oracle.simple_transfer(src_np, nchan, nslots, slot, seed=5)
+    f = xp.xp_fifo_create(nchan, nslots, slot)
+    xp.xp_fifo_set_lanes(f, 3)
+    xp.xp_fifo_set_discard(f, discard)
+    src = to_dev(torch, src_np)
+    dst = torch.zeros_like(src)
+    xp.xp_send_recv(f, src, dst, n, torch.cuda.current_stream())
+    assert xp.xp_fifo_status(f, True)[0] == xp.XP_OK
+    assert np.array_equal(from_dev(dst), want)
+    if not discard:
+        for c, fo in enumerate(fifos):
+            d = xp.xp_fifo_describe(f, c)
+            got = raw_view(torch, d.slots, nslots * slot, "|u1").cpu().numpy()
+            assert np.array_equal(got, fo.slots.reshape(-1))
+    xp.xp_fifo_destroy(f)
