@@ -151,20 +151,25 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
 xp_status xp_fifo_destroy(xp_fifo* f);
 
 /* CTAs per channel side: each channel's sender and receiver are each spread
- * over CTAs of one thread-block cluster that share the channel's one tail and
- * one head (default 1: one sender CTA and one receiver CTA per channel).
- * Sets the sender side to `lanes` (1 <= lanes <= 15) and the receiver side to
- * min(lanes, 16 - lanes); zero copy and direct posted transfers use one
- * receiver CTA, so up to 15 sender lanes serve them.  An operation whose
- * sender + receiver CTAs exceed 16 is refused (XP_ERR_INVALID).  SIMPLE FIFOs
- * only.  Takes effect at the next operation. */
+ * over CTAs ("lanes") that share the channel's one tail and one head (default
+ * 1: one sender CTA and one receiver CTA per channel).  Sets the sender side
+ * to `lanes` (1 <= lanes <= 32) and the receiver side to lanes if lanes <= 8,
+ * else to max(1, 16 - lanes); zero copy and direct posted transfers always use
+ * one receiver CTA.  HBM FIFOs: the lanes of a side meet on per-slot arrival
+ * counters in device memory, and an operation runs as one cooperative grid
+ * when nchannels x (sender + receiver CTAs) are resident on the GPU at once,
+ * else as one thread-block cluster per channel, which needs sender + receiver
+ * CTAs <= 16; an operation that fits neither way is refused (XP_ERR_INVALID).
+ * Host-placed FIFOs always use clusters.  SIMPLE FIFOs only.  Takes effect at
+ * the next operation. */
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
 
 /* Receiver CTAs per channel of xp_send_recv, independently of the sender's
- * (1 <= rlanes, lanes + rlanes <= 16): the slot-step is published whole, so
- * the receiver may cut it into a different number of stripes (also for
- * copy-mode posted and proxy transfers).  Zero copy and direct posted
- * transfers always use one receiver CTA.  SIMPLE FIFOs only. */
+ * (1 <= rlanes <= 32; the launch rules of xp_fifo_set_lanes apply): the
+ * slot-step is published whole, so the receiver may cut it into a different
+ * number of stripes (also for copy-mode posted and proxy transfers).  Zero
+ * copy and direct posted transfers always use one receiver CTA.  SIMPLE FIFOs
+ * only. */
 xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes);
 
 /* Whether receivers that read FIFO slots in HBM drop each 128-byte line of
