@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import shutil
 import statistics
@@ -153,6 +154,26 @@ def time_events(torch, stream, fn, iters):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+class OneCore:
+    """Runs the enclosed code on one host core (the oracle is a
+    single-threaded program); describes the host for the JSON line."""
+
+    def __enter__(self):
+        self.saved = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+        if self.saved:
+            os.sched_setaffinity(0, {min(self.saved)})
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved:
+            os.sched_setaffinity(0, self.saved)
+        return False
+
+    @staticmethod
+    def host():
+        return f"pinned to 1 of {os.cpu_count()} {platform.machine()} host cores"
+
+
 def cpu_oracle_rate(budget_s: float):
     """The oracle on the 1 GiB multi-channel workload: whole channels (64 MiB
     each) in order until the budget is used; returns (GB/s, sample text)."""
@@ -160,18 +181,20 @@ def cpu_oracle_rate(budget_s: float):
     w = workloads.SIMPLE_MULTI
     src = workloads.normal_bf16_bits(w["nelems"], w["seed"]).view(np.uint8)
     per = len(src) // w["nchannels"]
-    t0 = time.perf_counter()
-    moved, nch = 0, 0
-    while time.perf_counter() - t0 < budget_s and nch < 4096:
-        c = nch % w["nchannels"]
-        piece = src[c * per:(c + 1) * per]
-        dst, _, _ = oracle.simple_transfer(piece, 1, w["nslots"], w["slot_bytes"], seed=nch)
-        if not np.array_equal(dst, piece):
-            raise RuntimeError("oracle transfer mismatch")
-        moved += len(piece)
-        nch += 1
-    dt = time.perf_counter() - t0
-    return moved / dt / 1e9, f"{nch} channel(s) x 64 MiB of the 1 GiB bf16 workload, 8 x 512 KiB slots, slot-granular seeded interleaving ({dt:.1f} s)"
+    with OneCore():
+        t0 = time.perf_counter()
+        moved, nch = 0, 0
+        while time.perf_counter() - t0 < budget_s and nch < 4096:
+            c = nch % w["nchannels"]
+            piece = src[c * per:(c + 1) * per]
+            dst, _, _ = oracle.simple_transfer(piece, 1, w["nslots"], w["slot_bytes"], seed=nch)
+            if not np.array_equal(dst, piece):
+                raise RuntimeError("oracle transfer mismatch")
+            moved += len(piece)
+            nch += 1
+        dt = time.perf_counter() - t0
+    return moved / dt / 1e9, (f"{nch} channel(s) x 64 MiB of the 1 GiB bf16 workload, 8 x 512 KiB slots, "
+                              f"slot-granular seeded interleaving ({dt:.1f} s, {OneCore.host()})")
 
 
 def reference_arm(args):
@@ -182,6 +205,7 @@ def reference_arm(args):
     w = workloads.SIMPLE_MULTI
     src = workloads.normal_bf16_bits(w["nelems"], w["seed"]).view(np.uint8)
     per = len(src) // w["nchannels"]
+    pin = OneCore().__enter__()
     # calibrate one channel, then size each step to fit ~90 s overall
     t0 = time.perf_counter()
     oracle.simple_transfer(src[:per // 8], 1, w["nslots"], w["slot_bytes"], seed=0)
@@ -198,9 +222,11 @@ def reference_arm(args):
         times.append(time.perf_counter() - t0)
         if not np.array_equal(dst, sample):
             raise RuntimeError("oracle transfer mismatch")
+    pin.__exit__(None, None, None)
     t = sum(times)
     value = nbytes * args.steps / t / 1e9
-    desc = f"first {nbytes} bytes of the 1 GiB bf16 workload per step, 16 channels of 8 x 512 KiB, slot-granular seeded interleaving"
+    desc = (f"first {nbytes} bytes of the 1 GiB bf16 workload per step, 16 channels of 8 x 512 KiB, "
+            f"slot-granular seeded interleaving, {OneCore.host()}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
