@@ -16,6 +16,8 @@
 
 namespace xp {
 
+constexpr int kLLBatch = 4;   // lines a receiver thread polls together
+
 __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
   __shared__ __align__(8) u64 bars[kMaxSlots];
   __shared__ u64 s_base;
@@ -97,22 +99,43 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
         const u64 nl = (nlines - first) < L ? (nlines - first) : L;
         const uint32_t flag = (uint32_t)(step + 1);
         const char* slot = slots + (step % N) * p.slot_bytes;
-        for (u64 i = tid; i < nl && !failed; i += T) {
-          u64 a, b;
+        // A thread's lines of the step are polled kLLBatch at a time, all
+        // loads in flight together; only lines whose flags are not there
+        // yet are loaded again.
+        for (u64 i0 = tid; i0 < nl && !failed; i0 += T * kLLBatch) {
+          u64 a[kLLBatch], b[kLLBatch];
+          unsigned todo = 0;
+#pragma unroll
+          for (int q = 0; q < kLLBatch; ++q)
+            if (i0 + q * T < nl) todo |= 1u << q;
           WaitClock clk;
           unsigned it = 0;
-          for (;;) {
-            ll_load(slot + 16 * i, a, b);
-            if ((uint32_t)(a >> 32) == flag && (uint32_t)(b >> 32) == flag) break;
-            if ((++it & 7u) == 0 && !clk.tick(w, XP_WAIT_LL_FLAG, (a >> 32) | ((b >> 32) << 32), flag)) {
+          while (todo) {
+#pragma unroll
+            for (int q = 0; q < kLLBatch; ++q)
+              if (todo & (1u << q)) ll_load(slot + 16 * (i0 + q * T), a[q], b[q]);
+            u64 seen = 0;   // the flags of a line still missing, for the report
+#pragma unroll
+            for (int q = 0; q < kLLBatch; ++q)
+              if (todo & (1u << q)) {
+                if ((uint32_t)(a[q] >> 32) == flag && (uint32_t)(b[q] >> 32) == flag) {
+                  __stcs(dst + first + i0 + q * T, make_uint2((uint32_t)a[q], (uint32_t)b[q]));
+                  todo &= ~(1u << q);
+                } else {
+                  seen = (a[q] >> 32) | ((b[q] >> 32) << 32);
+                }
+              }
+            if (todo && (++it & 7u) == 0 && !clk.tick(w, XP_WAIT_LL_FLAG, seen, flag)) {
               failed = 1;
               break;
             }
           }
-          if (!failed) __stcs(dst + first + i, make_uint2((uint32_t)a, (uint32_t)b));
         }
         failed = __any_sync(0xffffffffu, failed);
-        if (!failed && lane == 0) mbar_arrive_cluster(bar0 + 8u * (uint32_t)(step % N));
+        // The lines have been read (their values are in registers): the
+        // slot may be refilled, so the signal needs no ordering, and a
+        // release would wait for this warp's stores to dst.
+        if (!failed && lane == 0) mbar_arrive_cluster_relaxed(bar0 + 8u * (uint32_t)(step % N));
       }
     }
   } else if (run && warp == kCopyWarps && lane == 0 && !sender) {
