@@ -131,7 +131,10 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
         piece(sz, parts, my_piece, &b0, &b1);
         warp_copy<LD_L2, ST_STREAM>(slots + (step % N) * S + b0, p.dst + lo + off + b0, b1 - b0);
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(bar0 + 8u * (uint32_t)(step % N));
+        // the piece of the slot has been read (the values went to dst): the
+        // slot may be refilled, so no ordering is needed, and a release would
+        // wait for this warp's stores to dst
+        if (lane == 0) mbar_arrive_cluster_relaxed(bar0 + 8u * (uint32_t)(step % N));
       }
     }
   } else if (run && warp == kCopyWarps && lane == 0) {
