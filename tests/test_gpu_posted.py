@@ -121,20 +121,23 @@ def test_posted_operations_continue(env):
     xp.xp_fifo_destroy(fifo)
 
 
-@pytest.mark.parametrize("direct,lanes,rlanes", [(False, 6, 7), (True, 8, None)])
-def test_posted_workload(env, direct, lanes, rlanes):
-    # 1 GiB of bf16 normals through 16 channels of 8 x 512 KiB
+@pytest.mark.parametrize("direct,lanes,rlanes,discard", [(False, 6, 7, False), (False, 10, 8, True),
+                                                       (True, 8, None, False)])
+def test_posted_workload(env, direct, lanes, rlanes, discard):
+    # 1 GiB of bf16 normals through 16 channels of 8 x 512 KiB; 10 + 8 lanes
+    # with discards on and direct at 8 lanes are the bench.py rows
     torch, xp = env
     w = workloads.SIMPLE_MULTI
     src_np = workloads.normal_bf16_bits(w["nelems"], w["seed"]).view(np.uint8)
     want, chans, _ = oracle.posted_transfer(src_np, w["nchannels"], w["nslots"], w["slot_bytes"], seed=3,
                                             direct=direct)
     fifo = _fifo(xp, w["nchannels"], w["nslots"], w["slot_bytes"], lanes, rlanes)
+    xp.xp_fifo_set_discard(fifo, discard)
     src, dst, rep = _posted(torch, xp, fifo, src_np, direct)
     assert np.array_equal(from_dev(dst), want)
     assert rep.max_occupancy == w["nslots"]
     _check_state(torch, xp, fifo, chans, w["nslots"], w["slot_bytes"], dst.data_ptr(), direct,
-                 [0] * w["nchannels"], check_slots=not direct)
+                 [0] * w["nchannels"], check_slots=not (direct or discard))
     xp.xp_fifo_destroy(fifo)
 
 
@@ -176,7 +179,7 @@ def test_posted_refused_after_error_and_bad_fifos(env):
         xp.xp_fifo_destroy(f)
 
 
-@pytest.mark.parametrize("lanes,rlanes", [(1, 1), (3, 5)])
+@pytest.mark.parametrize("lanes,rlanes", [(1, 1), (3, 5), (10, 8)])
 def test_posted_copy_with_discard(env, lanes, rlanes):
     # with the receivers dropping read slot lines from L2, the delivered bytes,
     # posts and completions still equal the oracle's (the slots' final bytes

@@ -92,15 +92,22 @@ def test_simple_counters_continue(env):
     xp.xp_fifo_destroy(fifo)
 
 
-@pytest.mark.parametrize("lanes", [1, 4])
-def test_simple_multichannel_workload(env, lanes):
-    # 1 GiB of bf16 N(0,1), 16 channels of 8 x 512 KiB
+@pytest.mark.parametrize("lanes,rlanes", [(1, 1), (4, 4), (10, 8)])
+def test_simple_multichannel_workload(env, lanes, rlanes):
+    # 1 GiB of bf16 N(0,1), 16 channels of 8 x 512 KiB; 10 + 8 lanes with
+    # discards on is the configuration bench.py times, twice in a row
     torch, xp = env
     w = workloads.SIMPLE_MULTI
     src = _multi_input()
     want, _, _ = oracle.simple_transfer(src, w["nchannels"], w["nslots"], w["slot_bytes"], seed=2)
-    got, rep = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"], lanes=lanes)
-    assert np.array_equal(got, want)
+    fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
+    xp.xp_fifo_set_lanes(fifo, lanes)
+    xp.xp_fifo_set_recv_lanes(fifo, rlanes)
+    for _ in range(2):
+        got, rep = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"], fifo=fifo)
+        assert np.array_equal(got, want)
+        assert rep.max_occupancy <= w["nslots"]
+    xp.xp_fifo_destroy(fifo)
 
 
 @pytest.mark.parametrize("n,nchan,nslots,slot,lanes", [
@@ -129,12 +136,14 @@ def test_zero_copy_sweep(env, n, nchan, nslots, slot, lanes):
     xp.xp_fifo_destroy(fifo)
 
 
-def test_zero_copy_workload(env):
+@pytest.mark.parametrize("lanes", [7, 8, 12])
+def test_zero_copy_workload(env, lanes):
+    # 1 GiB; 8 and 12 lanes are the bench.py rows
     torch, xp = env
     w = workloads.SIMPLE_MULTI
     src = _multi_input()
     want, _, _ = oracle.zero_copy_transfer(src, w["nchannels"], w["nslots"], w["slot_bytes"], seed=2)
-    got, _ = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"], lanes=7, zero_copy=True)
+    got, _ = _run_simple(torch, xp, src, w["nchannels"], w["nslots"], w["slot_bytes"], lanes=lanes, zero_copy=True)
     assert np.array_equal(got, want)
 
 
