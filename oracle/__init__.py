@@ -1,9 +1,9 @@
 """CPU oracle for the FIFO data plane — TEST INFRASTRUCTURE ONLY.
 
 A plain, slow, single-threaded simulation of the collective transport's
-device-side producer/consumer protocol (SIMPLE slots with head/tail, LL lines
-with inline flags, zero copy through ptrExchange, the host-placed FIFO, and the
-virtual ring allreduce), written from the pages' descriptions.  It shares no
+device-side producer/consumer protocol (SIMPLE slots with head/tail, LL and
+LL128 lines with inline flags, zero copy through ptrExchange, the host-placed
+FIFO, and the virtual ring allreduce), written from the pages' descriptions.  It shares no
 code with the CUDA path and never imports it.
 
 Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s CPU-baseline /
@@ -11,8 +11,8 @@ reference leg may import or run anything in this package.  The library itself
 never routes through it: there is no CPU fallback.
 
 Entry points:
-* `simple_transfer`, `ll_transfer`, `zero_copy_transfer`, `posted_transfer`,
-  `ce_transfer`:
+* `simple_transfer`, `ll_transfer`, `ll128_transfer`, `zero_copy_transfer`,
+  `posted_transfer`, `ce_transfer`:
   move a buffer through C channels under a seeded random interleaving and
   return the result;
 * `ring_allreduce`: the ring as state machines; `ring_order_sum`: the plain
@@ -26,13 +26,13 @@ arithmetic rounded to fp32, against int64 sums for int32, against the
 fp64 sum within the standard error bound, and the pages' printed sizes and
 ring-neighbour example (tests/golden/).
 """
-from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, Deadlock, LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender,
+from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, Deadlock, LL128Fifo, LL128Receiver, LL128Sender, LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender,
                    ProtocolViolation, SimpleFifo, SimpleReceiver, SimpleSender, System, ZeroCopyChannel,
-                   ZeroCopyReceiver, ZeroCopySender, explore, ll_flag, run)
+                   ZeroCopyReceiver, ZeroCopySender, explore, ll128_flag, ll_flag, run)
 from .partition import (channel_byte_ranges, ring_channel_ranges, ring_chunk_elems, ring_next,
                         ring_prev, ring_rounds, ring_schedule, slot_steps)
 from .ring import ring_order_sum, ring_system
-from .transfer import (ce_transfer, ll_transfer, posted_transfer, ring_allreduce, simple_transfer,
+from .transfer import (ce_transfer, ll128_transfer, ll_transfer, posted_transfer, ring_allreduce, simple_transfer,
                        zero_copy_transfer)
 
 __all__ = [
@@ -43,4 +43,5 @@ __all__ = [
     "ring_system", "simple_transfer", "ll_transfer", "zero_copy_transfer", "ring_allreduce",
     "PostedChannel", "PostedSender", "PostedReceiver", "posted_transfer",
     "CEFifo", "CESender", "CEProxy", "CEReceiver", "ce_transfer",
+    "LL128Fifo", "LL128Sender", "LL128Receiver", "ll128_flag", "ll128_transfer",
 ]

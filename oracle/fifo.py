@@ -18,6 +18,10 @@ Protocol sources (page title, section):
   identical steps with the buffers and tail in host memory.
 * LL: "RDMA and GPUDirect" §4.1 — the data carries the flag and the receiver
   polls memory.  Line = 16 bytes {data0, flag0, data1, flag1}.
+* LL128: same section (the flag sits in the last bytes of what was written)
+  and §8 (GPUDirect flush: a visible flag does not by itself mean the data
+  written before it is visible).  Line = 128 bytes, 15 uint64 payload words
+  and a uint64 flag in the last 8 bytes.
 * initial counters: "NCCL transport setup", netTransport (head starts at 0
   outside shared-buffer mode) and the per-slot size word initialised to -1.
 
@@ -27,6 +31,10 @@ Readings where the pages are silent:
   memory never matches; LL still uses head for slot reuse and has no tail;
 * each 8-byte half {data, flag} of an LL line becomes visible on its own
   (a 16-byte line may be seen torn), in any order within a small window;
+* LL128 flag of every line of slot-step s is s + 1 as a full uint64; the
+  sender makes a batch of lines' payload visible before it writes their
+  flags, and the receiver reads a line's payload only after its flag; each
+  8-byte word becomes visible on its own, in any order;
 * zero copy: the receiver posts its address only into an empty ptrExchange;
   the sender writes chunks of at most S bytes, one tail per chunk, under the
   same credit rule; the receiver returns head per chunk; the sender empties
@@ -426,6 +434,248 @@ class LLReceiver(Actor):
 
     def state(self):
         return (self.step, self.line, self.pub, self.early)
+
+
+# --------------------------------------------------------------------------
+# LL128 ("RDMA and GPUDirect" §4: the data carries the flag in the buffer's
+# last bytes; §8, GPUDirect flush: seeing the flag does not by itself mean
+# the data before it has landed)
+# --------------------------------------------------------------------------
+
+LL128_LINE_BYTES = 128   # 16 uint64 words
+LL128_LINE_WORDS = 16
+LL128_DATA_WORDS = 15    # words 0..14 carry payload, word 15 is the flag
+
+
+def ll128_flag(step: int) -> int:
+    """Flag word of every line of slot-step `step`: step + 1 as a full
+    uint64 (zeroed memory never matches; no wrap within 2**64 steps)."""
+    return (step + 1) & 0xFFFFFFFFFFFFFFFF
+
+
+class LL128Fifo:
+    """Shared state of one LL128 channel: N slots of S bytes of 128-byte lines."""
+
+    def __init__(self, nslots: int, slot_bytes: int, step0: int = 0):
+        if nslots < 1 or slot_bytes < LL128_LINE_BYTES or slot_bytes % LL128_LINE_BYTES:
+            raise ValueError("LL128 slots hold whole 128-byte lines")
+        self.N = nslots
+        self.S = slot_bytes
+        self.L = slot_bytes // LL128_LINE_BYTES
+        self.lines = np.zeros((nslots, self.L, LL128_LINE_WORDS), np.uint64)   # visible memory
+        self.owner = np.full((nslots, self.L, LL128_LINE_WORDS), -1, np.int64)  # step that wrote each word
+        self.head = step0
+        self.started = step0
+        self.max_occupancy = 0
+
+    def check(self):
+        occ = self.started - self.head
+        if occ < 0 or occ > self.N:
+            raise ProtocolViolation(f"LL128 sender started {self.started} steps, head {self.head}, N {self.N}")
+        self.max_occupancy = max(self.max_occupancy, occ)
+
+    def state(self):
+        return (self.head, self.started, self.lines.tobytes(), self.owner.tobytes())
+
+
+@dataclass
+class _Piece:
+    slot: int
+    line: int
+    w0: int            # first word of the line this piece writes
+    values: tuple      # uint64 words
+    step: int
+
+
+def _ll128_lines(nwords: int, L: int, rel: int) -> int:
+    """Lines of relative slot-step `rel` for a channel of `nwords` payload words."""
+    left = nwords - rel * L * LL128_DATA_WORDS
+    return min(L, ceil_div(left, LL128_DATA_WORDS))
+
+
+class LL128Sender(Actor):
+    """Send words[lo:hi] (uint64) as LL128 lines.
+
+    Slot-step s carries payload words [s*L*15, (s+1)*L*15) of the channel;
+    line i of a step the next 15 of them, words past the end written as 0.
+    The sender writes the lines of a step in batches of at most `batch`
+    lines: every payload word enters a pending pool and becomes visible on
+    its own (8 bytes: the unit a store is atomic in; `piece_words` > 1
+    coarsens it to keep exhaustive searches small); only when every payload
+    word of the batch is visible (the fence) do the batch's flags enter the
+    pool.  `window` bounds the pending payload lines.
+    `fault`: "skip_credit" (no head check), "flag_with_data" (a line's flag
+    enters the pool together with its payload: no fence).
+    """
+
+    def __init__(self, fifo: LL128Fifo, words: np.ndarray, lo: int, hi: int, batch: int = 2, window: int = 2,
+                 piece_words: int = 1, fault: str | None = None):
+        self.f, self.words, self.lo, self.hi = fifo, words, lo, hi
+        self.nwords = hi - lo
+        self.base = fifo.started
+        self.nsteps = ceil_div(self.nwords, fifo.L * LL128_DATA_WORDS)
+        self.step = self.base
+        self.line = 0
+        self.granted = False
+        self.batch = batch
+        self.window = window
+        self.pw = piece_words
+        self.in_batch: list[tuple[int, int, int]] = []   # (slot, line, step) written, flag not yet issued
+        self.pending: list[_Piece] = []
+        self.fault = fault
+        self.name = f"ll128-send[{lo}:{hi}]"
+
+    def _lines_in(self, step):
+        return _ll128_lines(self.nwords, self.f.L, step - self.base)
+
+    def done(self):
+        return self.step >= self.base + self.nsteps and not self.pending and not self.in_batch
+
+    def _data_pending(self):
+        return sum(1 for p in self.pending if p.w0 < LL128_DATA_WORDS)
+
+    def choices(self):
+        opts = [("vis", i) for i in range(len(self.pending))]
+        if self.in_batch and self._data_pending() == 0:
+            opts.append(("fence",))
+        if (self.step < self.base + self.nsteps and len(self.in_batch) < self.batch
+                and all(st == self.step for (_, _, st) in self.in_batch)):
+            if not self.granted:
+                if self.fault == "skip_credit" or self.step < self.f.head + self.f.N:
+                    opts.append(("grant",))
+            elif self._data_pending() < self.window * ceil_div(LL128_DATA_WORDS, self.pw):
+                opts.append(("issue",))
+        return opts
+
+    def fire(self, choice):
+        if choice[0] == "grant":
+            self.granted = True
+            self.f.started = self.step + 1
+        elif choice[0] == "issue":
+            rel = self.step - self.base
+            g0 = (rel * self.f.L + self.line) * LL128_DATA_WORDS     # first payload word of the line
+            vals = [int(self.words[self.lo + g0 + j]) if g0 + j < self.nwords else 0
+                    for j in range(LL128_DATA_WORDS)]
+            k = self.step % self.f.N
+            for w0 in range(0, LL128_DATA_WORDS, self.pw):
+                self.pending.append(_Piece(k, self.line, w0, tuple(vals[w0:w0 + self.pw]), self.step))
+            if self.fault == "flag_with_data":
+                self.pending.append(_Piece(k, self.line, LL128_DATA_WORDS, (ll128_flag(self.step),), self.step))
+            else:
+                self.in_batch.append((k, self.line, self.step))
+            self.line += 1
+            if self.line == self._lines_in(self.step):
+                self.step += 1
+                self.line = 0
+                self.granted = False
+        elif choice[0] == "fence":
+            for (k, ln, st) in self.in_batch:
+                self.pending.append(_Piece(k, ln, LL128_DATA_WORDS, (ll128_flag(st),), st))
+            self.in_batch = []
+        else:
+            p = self.pending.pop(choice[1])
+            if p.step >= self.f.head + self.f.N:
+                raise ProtocolViolation(f"LL128 step {p.step} overwrites slot {p.slot} before head {self.f.head}")
+            n = len(p.values)
+            self.f.lines[p.slot, p.line, p.w0:p.w0 + n] = np.array(p.values, np.uint64)
+            self.f.owner[p.slot, p.line, p.w0:p.w0 + n] = p.step
+
+    def state(self):
+        return (self.step, self.line, self.granted, tuple(self.in_batch),
+                tuple((p.slot, p.line, p.w0, p.values, p.step) for p in self.pending))
+
+
+class LL128Receiver(Actor):
+    """Receive LL128 lines into out[lo:hi] (uint64); head = step + 1 after a
+    slot's last line.
+
+    A line is read only once its flag word equals the step's flag, and the
+    read comes after the flag (the receiver's fence): every payload word it
+    takes must then have been written in this step.  `fault`:
+    "data_before_flag" (the payload words are loaded first and kept if the
+    flag then matches: no fence between), "head_early" (return credit before
+    reading the slot's last line).
+    """
+
+    def __init__(self, fifo: LL128Fifo, out: np.ndarray, lo: int, hi: int, fault: str | None = None):
+        self.f, self.out, self.lo, self.hi = fifo, out, lo, hi
+        self.nwords = hi - lo
+        self.base = fifo.head
+        self.nsteps = ceil_div(self.nwords, fifo.L * LL128_DATA_WORDS)
+        self.step = self.base
+        self.line = 0
+        self.pub = False
+        self.early = False
+        self.snap = None               # planted fault: payload loaded before the flag
+        self.fault = fault
+        self.name = f"ll128-recv[{lo}:{hi}]"
+
+    def _lines_in(self, step):
+        return _ll128_lines(self.nwords, self.f.L, step - self.base)
+
+    def done(self):
+        return self.step >= self.base + self.nsteps
+
+    def choices(self):
+        if self.done():
+            return []
+        if self.pub:
+            return [("head",)]
+        if (self.fault == "head_early" and not self.early
+                and self.line == self._lines_in(self.step) - 1):
+            return [("head",)]
+        if self.fault == "data_before_flag" and self.snap is None:
+            return [("load",)]
+        k = self.step % self.f.N
+        ok = int(self.f.lines[k, self.line, LL128_DATA_WORDS]) == ll128_flag(self.step)
+        if self.fault == "data_before_flag":
+            return [("read",)] if ok else [("drop",)]
+        return [("read",)] if ok else []
+
+    def _next_step(self):
+        self.step += 1
+        self.line = 0
+        self.pub = False
+        self.early = False
+
+    def fire(self, choice):
+        k = self.step % self.f.N
+        if choice[0] == "head":
+            self.f.head = self.step + 1
+            if self.pub:
+                self._next_step()
+            else:
+                self.early = True
+            return
+        if choice[0] == "load":
+            self.snap = (self.f.lines[k, self.line, :LL128_DATA_WORDS].copy(),
+                         self.f.owner[k, self.line, :LL128_DATA_WORDS].copy())
+            return
+        if choice[0] == "drop":
+            self.snap = None
+            return
+        if self.snap is not None:
+            vals, own = self.snap
+            self.snap = None
+        else:
+            vals = self.f.lines[k, self.line, :LL128_DATA_WORDS]
+            own = self.f.owner[k, self.line, :LL128_DATA_WORDS]
+        g0 = ((self.step - self.base) * self.f.L + self.line) * LL128_DATA_WORDS
+        n = min(LL128_DATA_WORDS, self.nwords - g0)
+        stale = [int(o) for o in own if o != self.step]
+        if stale:
+            raise ProtocolViolation(f"LL128 line {self.line} of step {self.step} read with words from steps {stale}")
+        self.out[self.lo + g0:self.lo + g0 + n] = vals[:n]
+        self.line += 1
+        if self.line == self._lines_in(self.step):
+            if self.early:
+                self._next_step()
+            else:
+                self.pub = True
+
+    def state(self):
+        snap = None if self.snap is None else (self.snap[0].tobytes(), self.snap[1].tobytes())
+        return (self.step, self.line, self.pub, self.early, snap)
 
 
 # --------------------------------------------------------------------------

@@ -10,7 +10,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, LLFifo, LLReceiver, LLSender, PostedChannel,
+from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, LL128Fifo, LL128Receiver, LL128Sender, LLFifo,
+                   LLReceiver, LLSender, PostedChannel,
                    PostedReceiver, PostedSender, SimpleFifo, SimpleReceiver, SimpleSender, System, ZeroCopyChannel,
                    ZeroCopyReceiver, ZeroCopySender, run)
 from .partition import channel_byte_ranges
@@ -45,6 +46,25 @@ def ll_transfer(words: np.ndarray, nchannels: int, nslots: int, slot_bytes: int,
     for f, (lo, hi) in zip(fifos, channel_byte_ranges(4 * len(words), nchannels)):
         if hi > lo:
             actors += [LLSender(f, words, lo // 4, hi // 4, window=window), LLReceiver(f, out, lo // 4, hi // 4)]
+    ev = run(System(actors, fifos, [out]), seed=seed)
+    return out, fifos, ev
+
+
+def ll128_transfer(src: np.ndarray, nchannels: int, nslots: int, slot_bytes: int, seed: int = 0,
+                   fifos: list[LL128Fifo] | None = None, batch: int = 2, window: int = 2, piece_words: int = 1):
+    """LL128 copy of a buffer of whole 8-byte words; returns (out, fifos, events)."""
+    raw = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
+    if len(raw) % 8:
+        raise ValueError("LL128 moves whole 8-byte words")
+    words = raw.view(np.uint64)
+    out = np.zeros_like(words)
+    if fifos is None:
+        fifos = [LL128Fifo(nslots, slot_bytes) for _ in range(nchannels)]
+    actors = []
+    for f, (lo, hi) in zip(fifos, channel_byte_ranges(len(raw), nchannels)):
+        if hi > lo:
+            actors += [LL128Sender(f, words, lo // 8, hi // 8, batch=batch, window=window, piece_words=piece_words),
+                       LL128Receiver(f, out, lo // 8, hi // 8)]
     ev = run(System(actors, fifos, [out]), seed=seed)
     return out, fifos, ev
 
