@@ -393,7 +393,7 @@ def e2e_row(torch, xp, fifo, src_np, stream, iters=5, chunk=64 << 20):
             "ms_per_step": ms, "api": "xp_send_recv_staged", "chunk_bytes": chunk}
 
 
-ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "ce", "loopback", "ll", "host_fifo", "ring")
+ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "ce", "loopback", "ll", "ll128", "host_fifo", "ring")
 
 
 def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
@@ -537,6 +537,41 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         beta, alpha = np.polyfit(sizes, us, 1)          # us = alpha + beta * bytes
         res["ll"] = {"us_per_message_with_launch": sweep, "pingpong_one_way_us": ns / 2 / 20000 / 1e3,
                      "alpha_us": float(alpha), "beta_gbs": float(1e-3 / beta) if beta > 0 else None, "status": st}
+
+    if want("ll128"):
+        # LL128 (128-byte lines: 120 payload bytes and a flag word): the LL size
+        # sweep through one FIFO of 8 x 32 KiB of lines, and 1 GiB through
+        # 16 channels of 8 x 512 KiB (HBM bytes per payload byte: src read
+        # and dst write, plus 128/120 for each of the slot write and read)
+        wl = workloads.LL_SWEEP
+        f = xp.xp_fifo_create(1, wl["nslots"], wl["slot_bytes"], xp.XP_PROTO_LL128)
+        sweep = {}
+        for size in wl["sizes"]:
+            words = torch.from_numpy(workloads.uniform_u32(size // 4, wl["seed"])).to("cuda")
+            out_t = torch.empty_like(words)
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    xp.xp_send_recv(f, words, out_t, size, s)
+                t = time_events(torch, s, lambda: xp.xp_send_recv(f, words, out_t, size, s), 100)
+            sweep[str(size)] = statistics.median(t) * 1e3
+        st, _ = xp.xp_fifo_status(f, True)
+        xp.xp_fifo_destroy(f)
+        src = torch.from_numpy(workloads.normal_bf16_bits(w["nelems"], w["seed"])).to("cuda")
+        dst = torch.empty_like(src)
+        n = src.numel() * 2
+        f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                xp.xp_send_recv(f, src, dst, n, s)
+            t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 10)
+        st2, _ = xp.xp_fifo_status(f, True)
+        ms = statistics.median(t)
+        res["ll128"] = {"us_per_message_with_launch": sweep, "sweep_status": st,
+                        "multi_1GiB_16ch": {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms,
+                                            "frac_of_hbm": (2 + 2 * 128 / 120) * n / (ms * 1e-3) / 1e9 / hbm_peak,
+                                            "exact": bool(st2 == xp.XP_OK and torch.equal(dst, src))}}
+        xp.xp_fifo_destroy(f)
+        del src, dst
 
     if want("host_fifo"):
         # host-placed FIFO: 256 MiB fp32, 8 channels x 8 x 1 MiB in pinned host memory

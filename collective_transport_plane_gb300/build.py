@@ -12,8 +12,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libxp.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
-SOURCES = ["xp_api.cu", "xp_p2p.cu", "xp_p2p_tma.cu", "xp_ll.cu", "xp_ring.cu", "xp_ring_tma.cu", "xp_noalloc.cu",
-           "xp_proxy.cu"]
+SOURCES = ["xp_api.cu", "xp_p2p.cu", "xp_p2p_tma.cu", "xp_ll.cu", "xp_ll128.cu", "xp_ring.cu", "xp_ring_tma.cu",
+           "xp_noalloc.cu", "xp_proxy.cu"]
 HEADERS = ["xp_internal.h", "xp_device.cuh", "xp_proxy.h"]
 
 # --fmad=false and the default -ftz=false keep the ring's fp32 adds plain IEEE

@@ -23,6 +23,7 @@ void* p2p_tma_kernel_ptr(int mode);   // 0 SIMPLE, 1 zero copy, 2 posted copy, 3
 int p2p_tma_threads();
 int p2p_tma_smem();
 void* ll_kernel_ptr();
+void* ll128_kernel_ptr();
 void* ll_pingpong_kernel_ptr();
 void* ring_kernel_ptr(int dtype);
 void* ring_tma_kernel_ptr(int dtype);
@@ -379,7 +380,10 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
   if (nslots < 1 || nslots > xp::kMaxSlots) return fail(XP_ERR_INVALID, "nslots %d not in [1, 64]", nslots);
   if (slot_bytes == 0 || slot_bytes % 16 || slot_bytes > (1ull << 31))
     return fail(XP_ERR_INVALID, "slot_bytes %zu must be a non-zero multiple of 16, at most 2^31", slot_bytes);
-  if (proto != XP_PROTO_SIMPLE && proto != XP_PROTO_LL) return fail(XP_ERR_INVALID, "unknown protocol %d", (int)proto);
+  if (proto != XP_PROTO_SIMPLE && proto != XP_PROTO_LL && proto != XP_PROTO_LL128)
+    return fail(XP_ERR_INVALID, "unknown protocol %d", (int)proto);
+  if (proto == XP_PROTO_LL128 && slot_bytes % 128)
+    return fail(XP_ERR_INVALID, "LL128 slot_bytes %zu is not a multiple of 128-byte lines", slot_bytes);
   if (place != XP_PLACE_DEVICE && place != XP_PLACE_HOST_MAPPED) return fail(XP_ERR_INVALID, "unknown placement %d", (int)place);
   if ((unsigned long long)nchannels * nslots * slot_bytes > (1ull << 40)) return fail(XP_ERR_INVALID, "FIFO larger than 2^40 bytes");
   xp_status s = ensure_abort_word();
@@ -541,7 +545,8 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   if (posted && (f->proto != XP_PROTO_SIMPLE || f->place != XP_PLACE_DEVICE))
     return fail(XP_ERR_INVALID, "posted transfers need a SIMPLE FIFO in device memory");
   if (mode == kOpProxy && !f->pump) return fail(XP_ERR_INVALID, "the proxy mode is not enabled (xp_fifo_enable_ce)");
-  if (f->proto == XP_PROTO_LL && bytes % 8) return fail(XP_ERR_INVALID, "LL moves whole 8-byte lines: bytes %% 8 != 0");
+  if (f->proto != XP_PROTO_SIMPLE && bytes % 8)
+    return fail(XP_ERR_INVALID, "LL and LL128 move whole 8-byte words: bytes %% 8 != 0");
   xp_status s = check_device(f->cm);
   if (s != XP_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -568,8 +573,8 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   p.timeout_ns = g_timeout_ns.load();
   const void* kernel;
   int csize, block, smem = 0;
-  if (f->proto == XP_PROTO_LL) {
-    kernel = xp::ll_kernel_ptr();
+  if (f->proto != XP_PROTO_SIMPLE) {
+    kernel = f->proto == XP_PROTO_LL ? xp::ll_kernel_ptr() : xp::ll128_kernel_ptr();
     p.lanes = 1;
     csize = 2;
     block = xp::kLLThreads;
@@ -628,7 +633,8 @@ xp_status xp_send_recv_staged(xp_fifo* f, const void* host_src, void* host_dst, 
   if (!host_src || !host_dst || !dev_src || !dev_dst) return fail(XP_ERR_INVALID, "a buffer is NULL");
   if (chunk_bytes == 0) chunk_bytes = (size_t)64 << 20;
   if (chunk_bytes % 16) return fail(XP_ERR_INVALID, "chunk_bytes %zu is not a multiple of 16", chunk_bytes);
-  if (f->proto == XP_PROTO_LL && bytes % 8) return fail(XP_ERR_INVALID, "LL moves whole 8-byte lines: bytes %% 8 != 0");
+  if (f->proto != XP_PROTO_SIMPLE && bytes % 8)
+    return fail(XP_ERR_INVALID, "LL and LL128 move whole 8-byte words: bytes %% 8 != 0");
   xp_status s = check_device(f->cm);
   if (s != XP_OK) return s;
   if (!f->s_in) {

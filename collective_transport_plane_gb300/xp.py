@@ -15,7 +15,7 @@ import os
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libxp.so")
 
 XP_OK, XP_ERR_INVALID, XP_ERR_CUDA, XP_ERR_TIMEOUT, XP_ERR_BOUNDS, XP_ERR_ABORTED, XP_ERR_INTERNAL = range(7)
-XP_PROTO_SIMPLE, XP_PROTO_LL = 0, 1
+XP_PROTO_SIMPLE, XP_PROTO_LL, XP_PROTO_LL128 = 0, 1, 2
 XP_PLACE_DEVICE, XP_PLACE_HOST_MAPPED = 0, 1
 XP_U8, XP_U32, XP_I32, XP_F32, XP_BF16 = range(5)
 (XP_WAIT_NONE, XP_WAIT_HEAD, XP_WAIT_TAIL, XP_WAIT_PTR_EXCHANGE, XP_WAIT_LL_FLAG, XP_WAIT_SLOT_BARRIER,

@@ -72,8 +72,9 @@ typedef enum {
   XP_ERR_INTERNAL = 6
 } xp_status;
 
-/* Protocols ([transfer] copy mode = SIMPLE; [rdma] §4.1 flag-in-data = LL). */
-typedef enum { XP_PROTO_SIMPLE = 0, XP_PROTO_LL = 1 } xp_proto;
+/* Protocols ([transfer] copy mode = SIMPLE; [rdma] §4.1 flag-in-data = LL
+ * with 16-byte lines, LL128 with 128-byte lines). */
+typedef enum { XP_PROTO_SIMPLE = 0, XP_PROTO_LL = 1, XP_PROTO_LL128 = 2 } xp_proto;
 
 /* Where the FIFO (slots and counters) lives: device HBM, or pinned host
  * memory mapped into the device address space ([setup] shmTransport). */
@@ -111,7 +112,8 @@ typedef struct {
  * at +128, uint64 ptrExchange at +256, uint64 step base at +384 and int64
  * size words (one per slot, -1 = never written) at +512; slots points at
  * slot 0, slot k at slots + k * slot_stride.  LL slots hold 16-byte lines
- * {data0, flag0, data1, flag1} (uint32 each).  posted points at the
+ * {data0, flag0, data1, flag1} (uint32 each); LL128 slots hold 128-byte
+ * lines of 15 uint64 payload words and a uint64 flag (the last 8 bytes).  posted points at the
  * channel's receiver-driven credit FIFO (xp_send_recv_posted): 64 post
  * entries of 64 bytes {uint64 addr, uint64 size, uint64 idx, pad} at +0, 64
  * completion entries of 16 bytes {uint64 size, uint64 idx} at +4096 and the
@@ -139,7 +141,7 @@ typedef struct {
  * buffSize / N bytes; [rdma] §7.2: allocated once, reused by every
  * transfer).  Counters start at 0 and size words at -1.
  *   1 <= nchannels <= 64, 1 <= nslots <= 64, slot_bytes a non-zero multiple
- *   of 16 (LL: of 16-byte lines), nchannels * nslots * slot_bytes <= 2^40.
+ *   of 16 (LL128: of 128-byte lines), nchannels * nslots * slot_bytes <= 2^40.
  * The library owns the memory (cudaMalloc, or cudaHostAlloc(Mapped|Portable)
  * for XP_PLACE_HOST_MAPPED) and frees it in xp_fifo_destroy.  The FIFO is
  * bound to the device current at creation.  Errors: XP_ERR_INVALID (bad
@@ -194,8 +196,13 @@ xp_status xp_fifo_describe(const xp_fifo* f, int channel, xp_channel_desc* out);
  * tail > step (acquire), check the size word, copy out, publish head =
  * step + 1.  XP_PROTO_SIMPLE: any byte count; XP_PROTO_LL: bytes a multiple
  * of 8, sent as 16-byte lines {d0, flag, d1, flag} with flag = step + 1 and
- * no tail ([rdma] §4.1).  src and dst must not overlap.  bytes == 0 is a
- * no-op returning XP_OK. */
+ * no tail ([rdma] §4.1).  XP_PROTO_LL128: bytes a multiple of 8; slot-step
+ * s carries 15 * slot_bytes / 128 payload words, line i of it the next 15
+ * (zeros past the end) and the uint64 flag s + 1 in its last 8 bytes; the
+ * sender makes a batch of lines' payload visible (fence) before it writes
+ * their flags and the receiver reads a line only after its flag (fence); no
+ * tail.  src and dst must not overlap.  bytes == 0 is a no-op returning
+ * XP_OK. */
 xp_status xp_send_recv(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream);
 
 /* Zero-copy transfer ([transfer] zero copy, address known only at run time):

@@ -43,7 +43,8 @@ def test_status_strings(xp):
 
 @pytest.mark.parametrize("args", [
     (0, 8, 1024, 0, 0), (65, 8, 1024, 0, 0), (1, 0, 1024, 0, 0), (1, 65, 1024, 0, 0),
-    (1, 8, 0, 0, 0), (1, 8, 24, 0, 0), (1, 8, 1024, 2, 0), (1, 8, 1024, 0, 5), (64, 64, 1 << 31, 0, 0)])
+    (1, 8, 0, 0, 0), (1, 8, 24, 0, 0), (1, 8, 1024, 3, 0), (1, 8, 1024, 0, 5), (64, 64, 1 << 31, 0, 0),
+    (1, 8, 192, 2, 0)])
 def test_fifo_create_rejects_bad_arguments(xp, args):
     with pytest.raises(xp.XpError) as e:
         xp.xp_fifo_create(*args)
