@@ -559,18 +559,22 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         src = torch.from_numpy(workloads.normal_bf16_bits(w["nelems"], w["seed"])).to("cuda")
         dst = torch.empty_like(src)
         n = src.numel() * 2
-        f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
-        with torch.cuda.stream(s):
-            for _ in range(3):
-                xp.xp_send_recv(f, src, dst, n, s)
-            t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 10)
-        st2, _ = xp.xp_fifo_status(f, True)
-        ms = statistics.median(t)
-        res["ll128"] = {"us_per_message_with_launch": sweep, "sweep_status": st,
-                        "multi_1GiB_16ch": {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms,
-                                            "frac_of_hbm": (2 + 2 * 128 / 120) * n / (ms * 1e-3) / 1e9 / hbm_peak,
-                                            "exact": bool(st2 == xp.XP_OK and torch.equal(dst, src))}}
-        xp.xp_fifo_destroy(f)
+        multi = {}
+        for lanes in (1, 2, 4):
+            f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
+            xp.xp_fifo_set_lanes(f, lanes)
+            dst.zero_()
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    xp.xp_send_recv(f, src, dst, n, s)
+                t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 10)
+            st2, _ = xp.xp_fifo_status(f, True)
+            ms = statistics.median(t)
+            multi[f"lanes{lanes}"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms,
+                                      "frac_of_hbm": (2 + 2 * 128 / 120) * n / (ms * 1e-3) / 1e9 / hbm_peak,
+                                      "exact": bool(st2 == xp.XP_OK and torch.equal(dst, src))}
+            xp.xp_fifo_destroy(f)
+        res["ll128"] = {"us_per_message_with_launch": sweep, "sweep_status": st, "multi_1GiB_16ch": multi}
         del src, dst
 
     if want("host_fifo"):

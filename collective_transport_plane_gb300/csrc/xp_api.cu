@@ -24,6 +24,7 @@ int p2p_tma_threads();
 int p2p_tma_smem();
 void* ll_kernel_ptr();
 void* ll128_kernel_ptr();
+int ll128_smem();
 void* ll_pingpong_kernel_ptr();
 void* ring_kernel_ptr(int dtype);
 void* ring_tma_kernel_ptr(int dtype);
@@ -491,7 +492,15 @@ xp_status xp_fifo_enable_ce(xp_fifo* f) {
 
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
-  if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
+  if (f->proto == XP_PROTO_LL128) {
+    // independent lanes: a cluster of a sender and a receiver CTA each, a
+    // head of its own each (lane 0: the channel's head word, lanes 1 .. 7:
+    // lines of the channel's arrival block)
+    if (lanes < 1 || lanes > 8) return fail(XP_ERR_INVALID, "LL128 lanes %d not in [1, 8]", lanes);
+    f->lanes = f->rlanes = lanes;
+    return XP_OK;
+  }
+  if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE and LL128 FIFOs only");
   if (lanes < 1 || lanes > xp::kMaxLanes) return fail(XP_ERR_INVALID, "lanes %d not in [1, 32]", lanes);
   f->lanes = lanes;
   f->rlanes = lanes <= xp::kMaxCluster / 2 ? lanes : (lanes < xp::kMaxCluster ? xp::kMaxCluster - lanes : 1);
@@ -575,9 +584,12 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   int csize, block, smem = 0;
   if (f->proto != XP_PROTO_SIMPLE) {
     kernel = f->proto == XP_PROTO_LL ? xp::ll_kernel_ptr() : xp::ll128_kernel_ptr();
-    p.lanes = 1;
+    // one cluster of a sender and a receiver CTA per channel (LL) or per
+    // lane of a channel (LL128)
+    p.lanes = f->proto == XP_PROTO_LL ? 1 : f->lanes;
     csize = 2;
     block = xp::kLLThreads;
+    if (f->proto == XP_PROTO_LL128) smem = xp::ll128_smem();
   } else {
     p.lanes = f->lanes;
     p.rlanes = (zero_copy || mode == kOpPostedDirect) ? 1 : f->rlanes;
@@ -605,7 +617,8 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     return fail(XP_ERR_INVALID, "%d channels x %d CTAs neither fit on the GPU at once nor form clusters of at most 16",
                 f->C, csize);
   XP_CUDA(cudaMemsetAsync(f->cm.status, 0, xp::kStatusClearBytes, st));
-  if ((s = launch(kernel, f->C * csize, block, launch_csize, &p, st, smem)) != XP_OK) return s;
+  const int grid = f->proto == XP_PROTO_SIMPLE ? f->C * csize : f->C * p.lanes * 2;
+  if ((s = launch(kernel, grid, block, launch_csize, &p, st, smem)) != XP_OK) return s;
   if (mode == kOpProxy) xp::pump_kick(f->pump);
   return record_done(f->cm, st);
 }

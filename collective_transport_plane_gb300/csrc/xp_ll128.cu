@@ -14,11 +14,17 @@
 // of once per line:
 //   sender   — store the payload of kBatch lines per thread, __syncwarp,
 //              fence (release), store the batch's flags;
-//   receiver — poll the batch's flags, fence (acquire), __syncwarp, load the
-//              batch's payload.
-// There is no tail; head returns slot credit.  One cluster of two CTAs per
-// channel (sender, receiver); the receiver's copy warps arrive on a per-slot
-// mbarrier and its publisher warp stores head.
+//   receiver — poll the batch's flags (one of them with acquire), __syncwarp,
+//              load the batch's payload.
+// There is no tail; head returns slot credit.  A channel runs on G
+// independent lanes, each a cluster of two CTAs (sender, receiver): lane g
+// owns the same fixed stripe of ceil(L / G) lines of every slot and keeps a
+// head of its own, so the lanes of a channel never wait for one another.
+// The receiver's copy warps arrive on a per-slot mbarrier and its publisher
+// warp stores the lane's head.  The last lane of a channel to finish an
+// operation moves the channel's step base on and sets every lane's head to
+// it, so the next operation may cut the slots into a different number of
+// stripes.
 #include <cuda_runtime.h>
 
 #include "xp_device.cuh"
@@ -30,6 +36,27 @@ namespace {
 constexpr u64 kLineBytes = 128;
 constexpr u64 kDataWords = 15;
 constexpr int kBatch = 8;          // lines per thread between two fences
+constexpr u64 kChunkLines = 32ull * kCopyWarps / 8 * kBatch;   // lines the copy warps write per stage
+// a stage holds a chunk's payload from the 16-byte boundary at or below its
+// first byte: at most 8 bytes of lead plus 120 bytes per line
+constexpr uint32_t kStageBytes = (uint32_t)((kChunkLines * 8 * kDataWords + 8 + 15) / 16 * 16);
+constexpr int kStages = 3;
+constexpr int kMaxLL128Lanes = 8;
+constexpr u64 kRowLines = 32ull * kCopyWarps / 8 * kLineBytes;   // bytes of slot between a thread's lines
+constexpr uint32_t kRowPayload = (uint32_t)(32ull * kCopyWarps / 8 * 8 * kDataWords);   // and of payload
+
+constexpr u64 kDirectBytes = 8192;   // chunks of less payload are read from src directly
+
+// End of the bulk-staged part [a0, end) of a chunk whose payload is bytes
+// [b0, b1) of src: the 16-byte boundary at or above b1 if that is still
+// inside the channel's range [., hi), else the one below; nothing is staged
+// for a short chunk, whose copy would only add the bulk copy's latency.
+__device__ __forceinline__ u64 staged_end(u64 b0, u64 b1, u64 hi) {
+  const u64 a0 = b0 & ~15ull;
+  if (b1 - b0 < kDirectBytes) return a0;
+  const u64 up = (b1 + 15) & ~15ull;
+  return up <= hi ? up : b1 & ~15ull;
+}
 
 __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void st_v2(void* p, u64 a, u64 b) {
@@ -46,6 +73,21 @@ __device__ __forceinline__ u64 ld_flag(const void* p) {
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ u64 ld_flag_acquire(const void* p) {
+  u64 v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ u64 atom_add_acq_rel(u64* p, u64 v) {
+  u64 old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ u64 ld_shared_u64(uint32_t saddr) {
+  u64 v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(saddr) : "memory");
+  return v;
+}
 __device__ __forceinline__ u64 ld_word(const void* p) {
   u64 v;
   asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -55,21 +97,33 @@ __device__ __forceinline__ u64 ld_word(const void* p) {
 }  // namespace
 
 __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p) {
+  extern __shared__ __align__(128) unsigned char stage_mem[];
   __shared__ __align__(8) u64 bars[kMaxSlots];
+  __shared__ __align__(8) u64 full[kStages], empty[kStages];
   __shared__ u64 s_base;
   __shared__ int s_stop;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const unsigned crank = cluster_ctarank();
-  const int ch = blockIdx.x / 2;
+  const unsigned G = (unsigned)p.lanes;
+  const unsigned pair = blockIdx.x / 2;
+  const int ch = (int)(pair / G);
+  const unsigned g = pair % G;                 // lane
   const bool sender = crank == 0;
   const u64 N = (u64)p.nslots;
   const u64 L = p.slot_bytes / kLineBytes;     // lines per slot
   const u64 W = L * kDataWords;                // payload words per slot-step
+  const u64 Lg = (L + G - 1) / G;              // stripe of lines per lane
+  const u64 l0 = g * Lg;
+  const u64 l1 = l0 + Lg < L ? l0 + Lg : L;
 
   char* ctl = p.ctl + (u64)ch * kCtlBytes;
-  u64* head = reinterpret_cast<u64*>(ctl + kHeadOff);
+  // lane 0's head is the channel's head word; lanes 1 .. 7 keep theirs on
+  // lines 1 .. 7 of the channel's block of the arrival region, whose line 0
+  // counts the lanes that have finished the operation
+  u64* arr = p.arr + (u64)ch * (kArrBytes / 8);
+  u64* head = g == 0 ? reinterpret_cast<u64*>(ctl + kHeadOff) : arr + 16 * g;
   u64* basew = reinterpret_cast<u64*>(ctl + kBaseOff);
   char* slots = p.slots + (u64)ch * p.ch_stride;
 
@@ -90,12 +144,19 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
       for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), kCopyWarps);
       mbar_init_fence();
     }
+    if (sender) {
+      for (int k = 0; k < kStages; ++k) {
+        mbar_init(smem_addr(&full[k]), 1);
+        mbar_init(smem_addr(&empty[k]), kCopyWarps);
+      }
+      mbar_init_fence();
+    }
   }
   cluster_sync_all();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
   ChanStats* cs = p.stats ? p.stats + ch : nullptr;
-  if (cs && sender && threadIdx.x == 0) {
+  if (cs && sender && g == 0 && threadIdx.x == 0) {
     const u64 t = globaltimer();
     cs->steps = run ? nsteps : 0;
     cs->t_start = t;
@@ -103,64 +164,108 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
     if (!run) cs->t_end = t;
   }
   // thread -> (line, 16-byte position in the line): a warp covers 4 lines
-  // per pass, the copy warps G lines; loops run per warp (wline), so the
-  // warp-wide barriers and votes inside them see every lane
-  constexpr u64 G = 32ull * kCopyWarps / 8;
-  const u64 wline = (u64)warp * 4;
+  // of the lane's stripe per pass, the copy warps P lines; loops run per
+  // warp (wline), so the warp-wide barriers and votes inside them see every
+  // lane
+  constexpr u64 P = 32ull * kCopyWarps / 8;
+  const u64 wline = l0 + (u64)warp * 4;
   const u64 sub = (threadIdx.x >> 3) & 3;
   const u64 pos = threadIdx.x & 7;
   const bool flag_lane = pos == 7;
 
   if (run && warp < kCopyWarps) {
-    const u64* src = reinterpret_cast<const u64*>(p.src + lo);
     u64* dst = reinterpret_cast<u64*>(p.dst + lo);
     if (sender) {
+      // The producer thread (below) stages each chunk of the lane's payload
+      // in shared memory with a bulk copy; the copy warps turn it into lines.
+      const uint32_t sm0 = smem_addr(stage_mem);
       u64 hcache = 0;
-      for (u64 s = 0; s < nsteps; ++s) {
+      u64 j = 0;           // chunks consumed
+      int failed = 0;
+      for (u64 s = 0; s < nsteps && !failed; ++s) {
         const u64 step = base + s;
         if (step + 1 > N && !warp_wait_geq(head, step + 1 - N, hcache, w, XP_WAIT_HEAD)) break;
         const u64 left = nwords - s * W;
-        const u64 nl = left >= W ? L : (left + kDataWords - 1) / kDataWords;
+        const u64 nla = left >= W ? L : (left + kDataWords - 1) / kDataWords;
+        const u64 nl = nla < l1 ? nla : l1;         // end of this lane's lines in the step
         const u64 flag = step + 1;
         char* slot = slots + (step % N) * p.slot_bytes;
-        const u64* ssrc = src + s * W;
-        for (u64 w0 = wline; w0 < nl; w0 += G * kBatch) {
-          const u64 i0 = w0 + sub;
-          // payload of up to kBatch lines: loads first, all in flight together
+        const u64 sbyte = lo + 8 * s * W;           // src offset of the step's first payload word
+        for (u64 c0 = l0; c0 < nl; c0 += kChunkLines, ++j) {
+          const int k = (int)(j % kStages);
+          if (!mbar_wait_cta(smem_addr(&full[k]), (uint32_t)((j / kStages) & 1), w)) {
+            failed = 1;
+            break;
+          }
+          const u64 c1 = c0 + kChunkLines < nl ? c0 + kChunkLines : nl;
+          const u64 wend = kDataWords * c1 < left ? kDataWords * c1 : left;
+          const u64 b0 = sbyte + 8 * kDataWords * c0;
+          const u64 a0 = b0 & ~15ull;
+          const u64 a1 = staged_end(b0, sbyte + 8 * wend, hi);   // staged: [a0, a1); a word past it is read directly
+          const u64 i0 = c0 + (u64)warp * 4 + sub;
+          const uint32_t stage = sm0 + k * kStageBytes;
+          if (c1 - c0 == kChunkLines && kDataWords * c1 <= left && sbyte + 8 * wend <= a1) {
+            // a whole chunk, all of it staged: fixed strides, no checks
+            const uint32_t so = stage + (uint32_t)(b0 - a0) + (uint32_t)(8 * kDataWords * ((u64)warp * 4 + sub) + 16 * pos);
+            char* line = slot + i0 * kLineBytes + 16 * pos;
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+              const u64 x = ld_shared_u64(so + q * kRowPayload);
+              if (flag_lane) {
+                st_u64(line + q * kRowLines, x);
+              } else {
+                st_v2(line + q * kRowLines, x, ld_shared_u64(so + q * kRowPayload + 8));
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local_relaxed(smem_addr(&empty[k]));
+            fence_gpu();
+            if (flag_lane) {
+#pragma unroll
+              for (int q = 0; q < kBatch; ++q) st_flag(line + 8 + q * kRowLines, flag);
+            }
+            continue;
+          }
           u64 a[kBatch], b[kBatch];
 #pragma unroll
           for (int q = 0; q < kBatch; ++q) {
-            const u64 i = i0 + q * G;
-            const u64 wd = i * kDataWords + 2 * pos;   // first payload word of this thread
+            const u64 i = i0 + q * P;
+            const u64 wd = i * kDataWords + 2 * pos;   // first payload word of this thread in the step
             a[q] = b[q] = 0;
-            if (i < nl) {
-              if (wd < left) a[q] = __ldcs(reinterpret_cast<const unsigned long long*>(ssrc + wd));
-              if (!flag_lane && wd + 1 < left) b[q] = __ldcs(reinterpret_cast<const unsigned long long*>(ssrc + wd + 1));
+            if (i < c1) {
+              const u64 g = sbyte + 8 * wd;
+              if (wd < left) a[q] = g < a1 ? ld_shared_u64(stage + (uint32_t)(g - a0))
+                                           : __ldcs(reinterpret_cast<const unsigned long long*>(p.src + g));
+              if (!flag_lane && wd + 1 < left)
+                b[q] = g + 8 < a1 ? ld_shared_u64(stage + (uint32_t)(g + 8 - a0))
+                                  : __ldcs(reinterpret_cast<const unsigned long long*>(p.src + g + 8));
             }
           }
 #pragma unroll
           for (int q = 0; q < kBatch; ++q) {
-            const u64 i = i0 + q * G;
-            if (i < nl) {
+            const u64 i = i0 + q * P;
+            if (i < c1) {
               char* line = slot + i * kLineBytes + 16 * pos;
               if (flag_lane) st_u64(line, a[q]);
               else st_v2(line, a[q], b[q]);
             }
           }
-          // every payload store of the warp's lines before any of their flags
+          // the stage's values are in registers (the stores above used them)
           __syncwarp();
+          if (lane == 0) mbar_arrive_local_relaxed(smem_addr(&empty[k]));
+          // every payload store of the warp's lines before any of their flags
           fence_gpu();
           if (flag_lane) {
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
-              const u64 i = i0 + q * G;
-              if (i < nl) st_flag(slot + i * kLineBytes + 8 * kDataWords, flag);
+              const u64 i = i0 + q * P;
+              if (i < c1) st_flag(slot + i * kLineBytes + 8 * kDataWords, flag);
             }
           }
         }
       }
     } else {
-      const uint32_t bar0 = smem_addr(&bars[0]);
+      const uint32_t bar0 = map_to_rank(smem_addr(&bars[0]), 1);
       int failed = 0;
       u64 hcache = 0;
       for (u64 r = 0; r < nsteps && !failed; ++r) {
@@ -169,60 +274,89 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
         // before that slot's previous phase has completed (head > step - N)
         if (r >= N && !warp_wait_geq(head, step + 1 - N, hcache, w, XP_WAIT_HEAD)) break;
         const u64 left = nwords - r * W;
-        const u64 nl = left >= W ? L : (left + kDataWords - 1) / kDataWords;
+        const u64 nla = left >= W ? L : (left + kDataWords - 1) / kDataWords;
+        const u64 nl = nla < l1 ? nla : l1;
         const u64 flag = step + 1;
         const char* slot = slots + (step % N) * p.slot_bytes;
         u64* sdst = dst + r * W;
-        for (u64 w0 = wline; w0 < nl && !failed; w0 += G * kBatch) {
+        for (u64 w0 = wline; w0 < nl && !failed; w0 += P * kBatch) {
           const u64 i0 = w0 + sub;
+          // this warp's lines of the batch all lie in the step and carry
+          // payload in every word: fixed strides, no checks
+          const bool whole = w0 + 3 + (kBatch - 1) * P < nl && kDataWords * (w0 + 4 + (kBatch - 1) * P) <= left;
+          const char* line = slot + i0 * kLineBytes + 16 * pos;
+          // Every flag of the batch is polled with relaxed loads, all in
+          // flight together, except the last line's (the anchor), which is
+          // loaded with acquire.  The sender warp that wrote these lines
+          // stored all of their payload before one fence and their flags
+          // after it, so the acquire that sees the anchor's flag makes the
+          // payload of every line of the batch visible to the loads below
+          // (the warp barrier passes that on to the other threads).
           int ok = 1;
           if (flag_lane) {
             unsigned todo = 0;
 #pragma unroll
             for (int q = 0; q < kBatch; ++q)
-              if (i0 + q * G < nl) todo |= 1u << q;
+              if (whole || i0 + q * P < nl) todo |= 1u << q;
+            const unsigned anchor = todo ? 1u << (31 - __clz(todo)) : 0u;
             WaitClock clk;
             unsigned it = 0;
             while (todo) {
               u64 seen = 0;
 #pragma unroll
               for (int q = 0; q < kBatch; ++q)
-                if (todo & (1u << q)) {
-                  const u64 f = ld_flag(slot + (i0 + q * G) * kLineBytes + 8 * kDataWords);
+                if ((todo & ~anchor) & (1u << q)) {
+                  const u64 f = ld_flag(line + 8 + q * kRowLines);
                   if (f == flag) todo &= ~(1u << q);
                   else seen = f;
                 }
+              if (todo & anchor) {
+                const u64 f = ld_flag_acquire(line + 8 + (31 - __clz(anchor)) * kRowLines);
+                if (f == flag) todo &= ~anchor;
+                else seen = f;
+              }
               if (todo && (++it & 7u) == 0 && !clk.tick(w, XP_WAIT_LL_FLAG, seen, flag)) {
                 ok = 0;
                 break;
               }
             }
           }
-          // the flag loads, then the payload loads of every thread of the warp
-          fence_gpu();
           __syncwarp();
           if (__any_sync(0xffffffffu, !ok)) {
             failed = 1;
             break;
           }
           u64 a[kBatch], b[kBatch];
+          unsigned long long* d = reinterpret_cast<unsigned long long*>(sdst + i0 * kDataWords + 2 * pos);
+          if (whole) {
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+              if (flag_lane) a[q] = ld_word(line + q * kRowLines);
+              else ll_load(line + q * kRowLines, a[q], b[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+              __stcs(d + q * P * kDataWords, a[q]);
+              if (!flag_lane) __stcs(d + q * P * kDataWords + 1, b[q]);
+            }
+            continue;
+          }
 #pragma unroll
           for (int q = 0; q < kBatch; ++q) {
-            const u64 i = i0 + q * G;
+            const u64 i = i0 + q * P;
             a[q] = b[q] = 0;
             if (i < nl) {
-              const char* line = slot + i * kLineBytes + 16 * pos;
-              if (flag_lane) a[q] = ld_word(line);
-              else ll_load(line, a[q], b[q]);
+              if (flag_lane) a[q] = ld_word(line + q * kRowLines);
+              else ll_load(line + q * kRowLines, a[q], b[q]);
             }
           }
 #pragma unroll
           for (int q = 0; q < kBatch; ++q) {
-            const u64 i = i0 + q * G;
+            const u64 i = i0 + q * P;
             const u64 wd = i * kDataWords + 2 * pos;
             if (i < nl) {
-              if (wd < left) __stcs(reinterpret_cast<unsigned long long*>(sdst + wd), a[q]);
-              if (!flag_lane && wd + 1 < left) __stcs(reinterpret_cast<unsigned long long*>(sdst + wd + 1), b[q]);
+              if (wd < left) __stcs(d + q * P * kDataWords, a[q]);
+              if (!flag_lane && wd + 1 < left) __stcs(d + q * P * kDataWords + 1, b[q]);
             }
           }
         }
@@ -232,6 +366,34 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
         if (!failed && lane == 0) mbar_arrive_cluster_relaxed(bar0 + 8u * (uint32_t)(step % N));
       }
     }
+  } else if (run && warp == kCopyWarps && lane == 0 && sender) {
+    // producer: stage chunk j of the lane's payload in stage j % kStages once
+    // the copy warps have released that stage's previous chunk.  Reading src
+    // needs no slot credit, so it runs up to kStages chunks ahead.
+    const uint32_t sm0 = smem_addr(stage_mem);
+    const u64 pol = policy_evict_first();
+    u64 j = 0;
+    bool ok = true;
+    for (u64 s = 0; s < nsteps && ok; ++s) {
+      const u64 left = nwords - s * W;
+      const u64 nla = left >= W ? L : (left + kDataWords - 1) / kDataWords;
+      const u64 nl = nla < l1 ? nla : l1;
+      const u64 sbyte = lo + 8 * s * W;
+      for (u64 c0 = l0; c0 < nl; c0 += kChunkLines, ++j) {
+        const int k = (int)(j % kStages);
+        if (j >= kStages && !mbar_wait_cta(smem_addr(&empty[k]), (uint32_t)(((j / kStages) - 1) & 1), w)) {
+          ok = false;
+          break;
+        }
+        const u64 c1 = c0 + kChunkLines < nl ? c0 + kChunkLines : nl;
+        const u64 wend = kDataWords * c1 < left ? kDataWords * c1 : left;
+        const u64 a0 = (sbyte + 8 * kDataWords * c0) & ~15ull;
+        const u64 a1 = staged_end(sbyte + 8 * kDataWords * c0, sbyte + 8 * wend, hi);
+        const uint32_t nb = a1 > a0 ? (uint32_t)(a1 - a0) : 0u;
+        mbar_arrive_expect_tx(smem_addr(&full[k]), nb);
+        if (nb) bulk_load(sm0 + k * kStageBytes, p.src + a0, nb, smem_addr(&full[k]), pol);
+      }
+    }
   } else if (run && warp == kCopyWarps && lane == 0 && !sender) {
     u64 r = 0;
     for (; r < nsteps; ++r) {
@@ -239,13 +401,25 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
       if (!mbar_wait(smem_addr(&bars[step % N]), (uint32_t)((r / N) & 1), w, XP_WAIT_SLOT_BARRIER, step)) break;
       st_release(head, step + 1);
     }
-    if (r == nsteps) st_relaxed(basew, base + nsteps);
-    if (cs) cs->t_end = globaltimer();
+    if (r == nsteps) {
+      // every lane has read the step base at its start; the last one to
+      // finish moves it on and leaves every lane's head there
+      const u64 done = atom_add_acq_rel(arr, 1);
+      if (done + 1 == G) {
+        const u64 nb = base + nsteps;
+        st_relaxed(reinterpret_cast<u64*>(ctl + kHeadOff), nb);
+        for (int h = 1; h < kMaxLL128Lanes; ++h) st_relaxed(arr + 16 * h, nb);
+        st_relaxed(basew, nb);
+        st_relaxed(arr, 0);
+        if (cs) cs->t_end = globaltimer();
+      }
+    }
   }
   __syncwarp();
   cluster_sync_all();
 }
 
 void* ll128_kernel_ptr() { return reinterpret_cast<void*>(&ll128_kernel); }
+int ll128_smem() { return kStages * (int)kStageBytes; }
 
 }  // namespace xp

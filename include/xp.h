@@ -162,8 +162,13 @@ xp_status xp_fifo_destroy(xp_fifo* f);
  * when nchannels x (sender + receiver CTAs) are resident on the GPU at once,
  * else as one thread-block cluster per channel, which needs sender + receiver
  * CTAs <= 16; an operation that fits neither way is refused (XP_ERR_INVALID).
- * Host-placed FIFOs always use clusters.  SIMPLE FIFOs only.  Takes effect at
- * the next operation. */
+ * Host-placed FIFOs always use clusters.  LL128 FIFOs: 1 <= lanes <= 8
+ * independent lanes per channel, each a cluster of a sender and a receiver
+ * CTA with a head of its own, lane g moving the same fixed stripe of
+ * ceil(L / lanes) of each slot's L lines; at the end of an operation every
+ * lane's head equals the channel's step base, so the count may change from
+ * one operation to the next.  LL FIFOs: refused.  Takes effect at the next
+ * operation. */
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
 
 /* Receiver CTAs per channel of xp_send_recv, independently of the sender's

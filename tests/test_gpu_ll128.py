@@ -84,11 +84,13 @@ SWEEP = [(8, 3, 1, 128), (120, 1, 1, 128), (1000, 3, 2, 256), (4096 + 8, 5, 3, 3
          (300008, 5, 3, 4096), (1 << 20, 2, 8, 32768), ((2 << 20) + 24, 1, 2, 512 << 10), (129 * 120, 2, 4, 128)]
 
 
+@pytest.mark.parametrize("lanes", [1, 3])
 @pytest.mark.parametrize("n,nchan,nslots,slot", SWEEP)
-def test_ll128_sweep(env, n, nchan, nslots, slot):
+def test_ll128_sweep(env, n, nchan, nslots, slot, lanes):
     torch, xp = env
     src = workloads.uniform_bytes(n, seed=n % 97)
     fifo = xp.xp_fifo_create(nchan, nslots, slot, xp.XP_PROTO_LL128)
+    xp.xp_fifo_set_lanes(fifo, lanes)
     fifos = None
     for k in range(2):
         want, fifos, _ = oracle.ll128_transfer(src, nchan, nslots, slot, seed=k, fifos=fifos)
@@ -97,17 +99,35 @@ def test_ll128_sweep(env, n, nchan, nslots, slot):
     xp.xp_fifo_destroy(fifo)
 
 
-def test_ll128_host_placed(env):
+@pytest.mark.parametrize("lanes", [1, 2])
+def test_ll128_host_placed(env, lanes):
     torch, xp = env
     src = workloads.uniform_bytes(200000, seed=5)
     fifo = xp.xp_fifo_create(2, 4, 4096, xp.XP_PROTO_LL128, xp.XP_PLACE_HOST_MAPPED)
+    xp.xp_fifo_set_lanes(fifo, lanes)
     want, fifos, _ = oracle.ll128_transfer(src, 2, 4, 4096, seed=2)
     assert np.array_equal(_ll128(torch, xp, fifo, src), want.view(np.uint8))
     _check_slots(torch, xp, fifo, fifos, 4, 4096)
     xp.xp_fifo_destroy(fifo)
 
 
-def test_ll128_workload(env):
+def test_ll128_lanes_change_between_operations(env):
+    # the lanes share the channel's head and step base, so the stripes may
+    # be cut differently from one operation to the next
+    torch, xp = env
+    fifo = xp.xp_fifo_create(3, 2, 1024, xp.XP_PROTO_LL128)
+    fifos = None
+    for i, lanes in enumerate((1, 4, 2, 8, 3, 1)):
+        src = workloads.uniform_bytes(20000 + 968 * i, seed=30 + i)
+        xp.xp_fifo_set_lanes(fifo, lanes)
+        want, fifos, _ = oracle.ll128_transfer(src, 3, 2, 1024, seed=i, fifos=fifos)
+        assert np.array_equal(_ll128(torch, xp, fifo, src), want.view(np.uint8)), lanes
+        _check_slots(torch, xp, fifo, fifos, 2, 1024)
+    xp.xp_fifo_destroy(fifo)
+
+
+@pytest.mark.parametrize("lanes", [1, 4])
+def test_ll128_workload(env, lanes):
     # 1 GiB of bf16 normals through 16 channels of 8 x 512 KiB LL128 slots:
     # identity, and the slots of the first and last channel by the format's
     # definition
@@ -115,6 +135,7 @@ def test_ll128_workload(env):
     w = workloads.SIMPLE_MULTI
     src_np = workloads.normal_bf16_bits(w["nelems"], w["seed"]).view(np.uint8)
     fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
+    xp.xp_fifo_set_lanes(fifo, lanes)
     assert np.array_equal(_ll128(torch, xp, fifo, src_np), src_np)
     words = src_np.view(np.uint64)
     ranges = oracle.channel_byte_ranges(src_np.nbytes, w["nchannels"])
@@ -140,7 +161,8 @@ def test_ll128_argument_errors(env):
                  lambda: xp.xp_send_recv_zero_copy(f, a, b, 64, torch.cuda.current_stream()),
                  lambda: xp.xp_send_recv_posted(f, a, b, 64, False, torch.cuda.current_stream()),
                  lambda: xp.xp_fifo_enable_ce(f),
-                 lambda: xp.xp_fifo_set_lanes(f, 2)):
+                 lambda: xp.xp_fifo_set_lanes(f, 9),
+                 lambda: xp.xp_fifo_set_recv_lanes(f, 2)):
         with pytest.raises(xp.XpError) as e:
             call()
         assert e.value.status == xp.XP_ERR_INVALID
@@ -162,7 +184,8 @@ def test_ll128_flag_wait_times_out(env):
     xp.xp_send_recv(fifo, src, out, 4096)
     st, rep = xp.xp_fifo_status(fifo, True)
     assert st == xp.XP_ERR_TIMEOUT
-    assert rep.where in (xp.XP_WAIT_HEAD, xp.XP_WAIT_LL_FLAG)
+    # whichever of the three stuck waits runs out first reports
+    assert rep.where in (xp.XP_WAIT_HEAD, xp.XP_WAIT_LL_FLAG, xp.XP_WAIT_SLOT_BARRIER)
     xp.xp_fifo_reset(fifo)
     xp.xp_set_spin_timeout_ns(2_000_000_000)
     xp.xp_send_recv(fifo, src, out, 4096)
