@@ -255,7 +255,7 @@ def main():
     ap.add_argument("--rows", default="",
                     help="profiling only: run just these comma-separated row groups (" + ",".join(ROW_GROUPS) +
                          ") after the step, without the end-to-end and CPU legs")
-    ap.add_argument("--mode", default="simple", choices=["simple", "zero_copy", "posted_copy", "posted_direct"],
+    ap.add_argument("--mode", default="simple", choices=["simple", "zero_copy", "posted_copy", "posted_direct", "ll128"],
                     help="profiling only: the transfer the timed step runs (the headline is simple)")
     ap.add_argument("--ring-mib", type=int, default=0,
                     help="profiling only: MiB per rank of the ring row instead of 256")
@@ -284,11 +284,15 @@ def main():
     src = torch.from_numpy(src_np).to("cuda")
     dst = torch.empty_like(src)
     stream = torch.cuda.Stream()
-    fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
-    xp.xp_fifo_set_lanes(fifo, args.lanes)
-    xp.xp_fifo_set_recv_lanes(fifo, args.rlanes)
+    if args.mode == "ll128":
+        fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
+        xp.xp_fifo_set_lanes(fifo, min(args.lanes, 8))
+    else:
+        fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
+        xp.xp_fifo_set_lanes(fifo, args.lanes)
+        xp.xp_fifo_set_recv_lanes(fifo, args.rlanes)
 
-    if args.mode == "simple":
+    if args.mode in ("simple", "ll128"):
         def step():
             xp.xp_send_recv(fifo, src, dst, nbytes, stream)
     elif args.mode == "zero_copy":
@@ -299,7 +303,7 @@ def main():
 
         def step():
             xp.xp_send_recv_posted(fifo, src, dst, nbytes, direct, stream)
-    per_byte = 2 if args.mode in ("zero_copy", "posted_direct") else 4
+    per_byte = {"zero_copy": 2, "posted_direct": 2, "ll128": 2 + 2 * 128 / 120}.get(args.mode, 4)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -335,15 +339,18 @@ def main():
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": "SIMPLE multi-channel: 1 GiB bf16 N(0,1) seed 2, 16 channels x 8 slots x 512 KiB, FIFO in HBM",
                    "nchannels": w["nchannels"], "nslots": w["nslots"], "slot_bytes": w["slot_bytes"],
-                   "sender_ctas_per_channel": args.lanes, "receiver_ctas_per_channel": args.rlanes,
+                   "sender_ctas_per_channel": min(args.lanes, 8) if args.mode == "ll128" else args.lanes,
+                   "receiver_ctas_per_channel": min(args.lanes, 8) if args.mode == "ll128" else args.rlanes,
                    "payload_bytes": nbytes, "parallelism": f"replicas{world}",
                    "l2": "inputs (1 GiB) larger than L2; the 64 MiB FIFO itself is L2-resident by design"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": profiled_traffic() if args.mode == "simple" else None,
                      "peak_kind": f"{peak_kind} HBM copy (burst)",
-                     "accounting": "4 bytes per payload byte: src read, slot write, slot read, dst write"
-                                   if per_byte == 4 else "2 bytes per payload byte: src read, dst write"},
+                     "accounting": {4: "4 bytes per payload byte: src read, slot write, slot read, dst write",
+                                    2: "2 bytes per payload byte: src read, dst write"}.get(
+                                        per_byte, "2 + 2 x 128/120 bytes per payload byte: src read, dst write, "
+                                                  "and 128-byte lines of 120 payload bytes written and read")},
         "clocks": clk,
     }
 
