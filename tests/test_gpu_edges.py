@@ -55,6 +55,46 @@ def test_max_channels_and_slots(env, mode):
     xp.xp_fifo_destroy(f)
 
 
+@pytest.mark.parametrize("lanes", [1, 8])
+def test_ll128_max_channels_and_slots(env, lanes):
+    # 64 channels x 64 one-line slots, every channel wrapping its FIFO 3
+    # times; at 8 lanes most lanes own no line, and the 1024 CTAs run in
+    # waves (the lanes never wait for one another)
+    torch, xp = env
+    C, N, S = 64, 64, 128
+    n = C * N * 120 * 3 + 8
+    f = xp.xp_fifo_create(C, N, S, xp.XP_PROTO_LL128)
+    xp.xp_fifo_set_lanes(f, lanes)
+    src_np = workloads.uniform_bytes(n, seed=65)
+    want = oracle.ll128_transfer(src_np, C, N, S, seed=1)[0].view(np.uint8)
+    src = to_dev(torch, src_np)
+    dst = torch.zeros_like(src)
+    xp.xp_send_recv(f, src, dst, n, torch.cuda.current_stream())
+    st, rep = xp.xp_fifo_status(f, True)
+    assert st == xp.XP_OK, (st, rep.channel, rep.where)
+    assert np.array_equal(from_dev(dst), want)
+    xp.xp_fifo_destroy(f)
+
+
+def test_ll128_large_slot(env):
+    # one channel of 2 slots of 512 MiB of lines (480 MiB of payload each)
+    # at 8 lanes: 1.5 GiB moves in four slot-steps, the last one short, and
+    # wraps the FIFO; identity is the oracle's result for a copy of any size
+    torch, xp = env
+    S = 512 << 20
+    n = (3 << 29) - 8
+    src = torch.randint(0, 256, (n,), dtype=torch.uint8, device="cuda",
+                        generator=torch.Generator(device="cuda").manual_seed(7))
+    dst = torch.zeros_like(src)
+    f = xp.xp_fifo_create(1, 2, S, xp.XP_PROTO_LL128)
+    xp.xp_fifo_set_lanes(f, 8)
+    xp.xp_send_recv(f, src, dst, n, torch.cuda.current_stream())
+    st, rep = xp.xp_fifo_status(f, True)
+    assert st == xp.XP_OK, (st, rep.where)
+    assert torch.equal(dst, src)
+    xp.xp_fifo_destroy(f)
+
+
 def test_one_gib_slot(env):
     # a single channel of 2 slots of 1 GiB: 64-bit offsets inside one slot-step
     torch, xp = env

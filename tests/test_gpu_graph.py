@@ -32,19 +32,22 @@ def _capture(torch, fn):
     return g
 
 
-@pytest.mark.parametrize("mode", ["simple", "zero_copy", "posted_copy", "posted_direct", "ce"])
+@pytest.mark.parametrize("mode", ["simple", "zero_copy", "posted_copy", "posted_direct", "ce", "ll", "ll128"])
 def test_p2p_graph_replay(env, mode):
     torch, xp = env
-    nchan, nslots, slot, n = 4, 4, 8192, 300007
-    fifo = xp.xp_fifo_create(nchan, nslots, slot)
-    xp.xp_fifo_set_lanes(fifo, 2)
+    nchan, nslots, slot = 4, 4, 8192
+    n = 300008 if mode in ("ll", "ll128") else 300007
+    proto = {"ll": xp.XP_PROTO_LL, "ll128": xp.XP_PROTO_LL128}.get(mode, xp.XP_PROTO_SIMPLE)
+    fifo = xp.xp_fifo_create(nchan, nslots, slot, proto)
+    if mode != "ll":
+        xp.xp_fifo_set_lanes(fifo, 2)
     if mode == "ce":
         xp.xp_fifo_enable_ce(fifo)       # the pump keeps serving replays
     src = torch.zeros(n, dtype=torch.uint8, device="cuda")
     dst = torch.zeros_like(src)
 
     def op(s):
-        if mode == "simple":
+        if mode in ("simple", "ll", "ll128"):
             xp.xp_send_recv(fifo, src, dst, n, s)
         elif mode == "zero_copy":
             xp.xp_send_recv_zero_copy(fifo, src, dst, n, s)
@@ -58,6 +61,10 @@ def test_p2p_graph_replay(env, mode):
         src_np = workloads.uniform_bytes(n, seed=80 + i)
         if mode == "simple":
             want = oracle.simple_transfer(src_np, nchan, nslots, slot, seed=i)[0]
+        elif mode == "ll":
+            want = oracle.ll_transfer(src_np.view(np.uint32), nchan, nslots, slot, seed=i)[0].view(np.uint8)
+        elif mode == "ll128":
+            want = oracle.ll128_transfer(src_np, nchan, nslots, slot, seed=i)[0].view(np.uint8)
         elif mode == "zero_copy":
             want = oracle.zero_copy_transfer(src_np, nchan, nslots, slot, seed=i)[0]
         elif mode == "ce":
