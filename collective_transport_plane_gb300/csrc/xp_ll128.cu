@@ -204,17 +204,20 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
           const u64 a1 = staged_end(b0, sbyte + 8 * wend, hi);   // staged: [a0, a1); a word past it is read directly
           const u64 i0 = c0 + (u64)warp * 4 + sub;
           const uint32_t stage = sm0 + k * kStageBytes;
-          if (c1 - c0 == kChunkLines && kDataWords * c1 <= left && sbyte + 8 * wend <= a1) {
-            // a whole chunk, all of it staged: fixed strides, no checks
+          if (kDataWords * c1 <= left && sbyte + 8 * wend <= a1) {
+            // every line of the chunk is whole payload and staged: fixed
+            // strides, one check per line
             const uint32_t so = stage + (uint32_t)(b0 - a0) + (uint32_t)(8 * kDataWords * ((u64)warp * 4 + sub) + 16 * pos);
             char* line = slot + i0 * kLineBytes + 16 * pos;
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
-              const u64 x = ld_shared_u64(so + q * kRowPayload);
-              if (flag_lane) {
-                st_u64(line + q * kRowLines, x);
-              } else {
-                st_v2(line + q * kRowLines, x, ld_shared_u64(so + q * kRowPayload + 8));
+              if (i0 + q * P < c1) {
+                const u64 x = ld_shared_u64(so + q * kRowPayload);
+                if (flag_lane) {
+                  st_u64(line + q * kRowLines, x);
+                } else {
+                  st_v2(line + q * kRowLines, x, ld_shared_u64(so + q * kRowPayload + 8));
+                }
               }
             }
             __syncwarp();
@@ -222,7 +225,8 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
             fence_gpu();
             if (flag_lane) {
 #pragma unroll
-              for (int q = 0; q < kBatch; ++q) st_flag(line + 8 + q * kRowLines, flag);
+              for (int q = 0; q < kBatch; ++q)
+                if (i0 + q * P < c1) st_flag(line + 8 + q * kRowLines, flag);
             }
             continue;
           }
@@ -281,9 +285,9 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
         u64* sdst = dst + r * W;
         for (u64 w0 = wline; w0 < nl && !failed; w0 += P * kBatch) {
           const u64 i0 = w0 + sub;
-          // this warp's lines of the batch all lie in the step and carry
-          // payload in every word: fixed strides, no checks
-          const bool whole = w0 + 3 + (kBatch - 1) * P < nl && kDataWords * (w0 + 4 + (kBatch - 1) * P) <= left;
+          // every line of the step up to nl carries payload in every word:
+          // fixed strides, one check per line
+          const bool whole = kDataWords * nl <= left;
           const char* line = slot + i0 * kLineBytes + 16 * pos;
           // Every flag of the batch is polled with relaxed loads, all in
           // flight together, except the last line's (the anchor), which is
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
             unsigned todo = 0;
 #pragma unroll
             for (int q = 0; q < kBatch; ++q)
-              if (whole || i0 + q * P < nl) todo |= 1u << q;
+              if (i0 + q * P < nl) todo |= 1u << q;
             const unsigned anchor = todo ? 1u << (31 - __clz(todo)) : 0u;
             WaitClock clk;
             unsigned it = 0;
@@ -331,13 +335,18 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
           if (whole) {
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
-              if (flag_lane) a[q] = ld_word(line + q * kRowLines);
-              else ll_load(line + q * kRowLines, a[q], b[q]);
+              a[q] = b[q] = 0;
+              if (i0 + q * P < nl) {
+                if (flag_lane) a[q] = ld_word(line + q * kRowLines);
+                else ll_load(line + q * kRowLines, a[q], b[q]);
+              }
             }
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
-              __stcs(d + q * P * kDataWords, a[q]);
-              if (!flag_lane) __stcs(d + q * P * kDataWords + 1, b[q]);
+              if (i0 + q * P < nl) {
+                __stcs(d + q * P * kDataWords, a[q]);
+                if (!flag_lane) __stcs(d + q * P * kDataWords + 1, b[q]);
+              }
             }
             continue;
           }
