@@ -25,6 +25,7 @@ int p2p_tma_smem();
 void* ll_kernel_ptr();
 void* ll128_kernel_ptr();
 int ll128_smem();
+int ll128_threads();
 void* ll_pingpong_kernel_ptr();
 void* ring_kernel_ptr(int dtype);
 void* ring_tma_kernel_ptr(int dtype);
@@ -588,7 +589,7 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     // lane of a channel (LL128)
     p.lanes = f->proto == XP_PROTO_LL ? 1 : f->lanes;
     csize = 2;
-    block = xp::kLLThreads;
+    block = f->proto == XP_PROTO_LL ? xp::kLLThreads : xp::ll128_threads();
     if (f->proto == XP_PROTO_LL128) smem = xp::ll128_smem();
   } else {
     p.lanes = f->lanes;

@@ -33,17 +33,19 @@ namespace xp {
 
 namespace {
 
+constexpr int kL128Warps = 16;     // copy warps per CTA (one more warp: producer or publisher)
+constexpr int kL128Threads = 32 * (kL128Warps + 1);
 constexpr u64 kLineBytes = 128;
 constexpr u64 kDataWords = 15;
 constexpr int kBatch = 8;          // lines per thread between two fences
-constexpr u64 kChunkLines = 32ull * kCopyWarps / 8 * kBatch;   // lines the copy warps write per stage
+constexpr u64 kChunkLines = 32ull * kL128Warps / 8 * kBatch;   // lines the copy warps write per stage
 // a stage holds a chunk's payload from the 16-byte boundary at or below its
 // first byte: at most 8 bytes of lead plus 120 bytes per line
 constexpr uint32_t kStageBytes = (uint32_t)((kChunkLines * 8 * kDataWords + 8 + 15) / 16 * 16);
 constexpr int kStages = 3;
 constexpr int kMaxLL128Lanes = 8;
-constexpr u64 kRowLines = 32ull * kCopyWarps / 8 * kLineBytes;   // bytes of slot between a thread's lines
-constexpr uint32_t kRowPayload = (uint32_t)(32ull * kCopyWarps / 8 * 8 * kDataWords);   // and of payload
+constexpr u64 kRowLines = 32ull * kL128Warps / 8 * kLineBytes;   // bytes of slot between a thread's lines
+constexpr uint32_t kRowPayload = (uint32_t)(32ull * kL128Warps / 8 * 8 * kDataWords);   // and of payload
 
 constexpr u64 kDirectBytes = 8192;   // chunks of less payload are read from src directly
 
@@ -96,7 +98,7 @@ __device__ __forceinline__ u64 ld_word(const void* p) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p) {
+__global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams p) {
   extern __shared__ __align__(128) unsigned char stage_mem[];
   __shared__ __align__(8) u64 bars[kMaxSlots];
   __shared__ __align__(8) u64 full[kStages], empty[kStages];
@@ -141,13 +143,13 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
       if (atomicCAS(&p.status->code, 0, XP_ERR_ABORTED) == 0) p.status->where = XP_WAIT_STICKY;
     }
     if (!sender) {
-      for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), kCopyWarps);
+      for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), kL128Warps);
       mbar_init_fence();
     }
     if (sender) {
       for (int k = 0; k < kStages; ++k) {
         mbar_init(smem_addr(&full[k]), 1);
-        mbar_init(smem_addr(&empty[k]), kCopyWarps);
+        mbar_init(smem_addr(&empty[k]), kL128Warps);
       }
       mbar_init_fence();
     }
@@ -167,13 +169,13 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
   // of the lane's stripe per pass, the copy warps P lines; loops run per
   // warp (wline), so the warp-wide barriers and votes inside them see every
   // lane
-  constexpr u64 P = 32ull * kCopyWarps / 8;
+  constexpr u64 P = 32ull * kL128Warps / 8;
   const u64 wline = l0 + (u64)warp * 4;
   const u64 sub = (threadIdx.x >> 3) & 3;
   const u64 pos = threadIdx.x & 7;
   const bool flag_lane = pos == 7;
 
-  if (run && warp < kCopyWarps) {
+  if (run && warp < kL128Warps) {
     u64* dst = reinterpret_cast<u64*>(p.dst + lo);
     if (sender) {
       // The producer thread (below) stages each chunk of the lane's payload
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
         if (!failed && lane == 0) mbar_arrive_cluster_relaxed(bar0 + 8u * (uint32_t)(step % N));
       }
     }
-  } else if (run && warp == kCopyWarps && lane == 0 && sender) {
+  } else if (run && warp == kL128Warps && lane == 0 && sender) {
     // producer: stage chunk j of the lane's payload in stage j % kStages once
     // the copy warps have released that stage's previous chunk.  Reading src
     // needs no slot credit, so it runs up to kStages chunks ahead.
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
         if (nb) bulk_load(sm0 + k * kStageBytes, p.src + a0, nb, smem_addr(&full[k]), pol);
       }
     }
-  } else if (run && warp == kCopyWarps && lane == 0 && !sender) {
+  } else if (run && warp == kL128Warps && lane == 0 && !sender) {
     u64 r = 0;
     for (; r < nsteps; ++r) {
       const u64 step = base + r;
@@ -430,5 +432,6 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll128_kernel(const P2pParams p)
 
 void* ll128_kernel_ptr() { return reinterpret_cast<void*>(&ll128_kernel); }
 int ll128_smem() { return kStages * (int)kStageBytes; }
+int ll128_threads() { return kL128Threads; }
 
 }  // namespace xp
