@@ -246,8 +246,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--lanes", type=int, default=10, help="sender CTAs per channel")
-    ap.add_argument("--rlanes", type=int, default=8, help="receiver CTAs per channel")
+    ap.add_argument("--lanes", type=int, default=9, help="sender CTAs per channel")
+    ap.add_argument("--rlanes", type=int, default=9, help="receiver CTAs per channel")
     ap.add_argument("--no-rows", action="store_true", help="time the step only")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--mib", type=int, default=0,
@@ -428,7 +428,7 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
     if want("zero_copy"):
         # zero copy, 1 GiB through the same geometry
         zc = {}
-        for lanes in (8, 12):
+        for lanes in (7, 8):
             f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
             xp.xp_fifo_set_lanes(f, lanes)
             with torch.cuda.stream(s):
@@ -459,7 +459,7 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         # staging slots (4 bytes of HBM traffic per payload byte) and direct
         # mode into dst (2 bytes per payload byte)
         posted = {}
-        for direct, lanes, rl in ((False, 10, 8), (True, 8, None)):
+        for direct, lanes, rl in ((False, 9, 9), (True, 6, None)):
             f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
             xp.xp_fifo_set_lanes(f, lanes)
             if rl:

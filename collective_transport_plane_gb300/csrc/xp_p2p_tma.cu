@@ -57,6 +57,15 @@ constexpr uint32_t kTmaChunk = 32768;
 constexpr int kLookSend = 2;
 constexpr int kLookZeroCopy = 2;
 constexpr int kRecvStoresInFlight = 1;   // receiver: dst stores still reading their stage
+// The sender's fifth warp (idle otherwise; the receiver's discards) keeps
+// this many bulk entries of src beyond the mover's loads on their way into
+// L2 with cp.async.bulk.prefetch (no shared memory, no completion), so more
+// of the source is in flight than three stages hold.  The slot-filling
+// modes take one entry (two cost 3% there: the prefetched lines crowd the
+// L2-resident FIFO); zero copy and direct posts, which keep nothing in L2,
+// take two.
+constexpr int kPrefetchSlots = 1;
+constexpr int kPrefetchToUser = 2;
 // Receivers that read FIFO slots invalidate in L2, with discard.global.L2,
 // the 128-byte lines of their stripe that they have read, before returning
 // credit: the slot's dirty bytes are dead once read, and without this they are
@@ -175,6 +184,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   __shared__ u64 s_mirror;   // latest head / post (sender) or tail / completion (receiver) seen by the watcher
   __shared__ u64 s_done;     // sender: steps [0, s_done) have their bulk stores complete
   __shared__ u64 s_read;     // receiver: steps [0, s_read) have their slot stripe in shared memory
+  __shared__ u64 s_loaded;   // sender: bulk loads the mover has issued (~0: the mover is done)
   __shared__ u64 s_addr[kPosted ? kMaxSlots : 1];   // posted sender: address and size of each slot's post
   __shared__ u64 s_cap[kPosted ? kMaxSlots : 1];
   __shared__ int s_stop;
@@ -239,6 +249,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
     s_mirror = 0;
     s_done = 0;
     s_read = 0;
+    s_loaded = 0;
     for (int k = 0; k < kTmaStages; ++k) {
       mbar_init(smem_addr(&full[k]), 1);
       mbar_init(smem_addr(&empty[k]), 1);
@@ -337,7 +348,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           if (nb)
             bulk_load(sm0 + k * kTmaChunk, p.src + lo + s * S + st.b0 + e * kTmaChunk, nb, smem_addr(&full[k]), pol_user);
         };
+        volatile u64* loaded = &s_loaded;   // pacing for the prefetcher only
         for (; jl < total && jl < (u64)kLook; ++jl) issue_load(jl);
+        *loaded = jl;
         char* dstp = nullptr;
         if (kZeroCopy) {
           u64 v = 0;
@@ -393,6 +406,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
               // memory, it has finished
               bulk_wait_read<kTmaStages - kLook>();
               issue_load(jl++);
+              *loaded = jl;
             }
             if (pending >= 0 && ++since == kDefer) {
               bulk_wait<kDefer>();
@@ -413,6 +427,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           pending = (long long)s;
           since = 0;
         }
+        *loaded = ~0ull;
         bulk_wait<0>();
         if (ok && pending >= 0) {
           fence_proxy_async_global();
@@ -599,6 +614,35 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         ctl_store<kProxy>(basew, base + nsteps);
       }
       if (cs && !sender) cs->t_end = globaltimer();
+    }
+  }
+  if (run && sender && warp == 4 && lane == 0) {
+    // ---------------- prefetcher ----------------
+    // walks the mover's entries kPrefetch ahead of its bulk loads and asks
+    // L2 to fetch each from src; it only paces itself on the mover's count,
+    // so it needs no ordering, and it stops when the mover is done, on the
+    // operation's abort flag, or after timeout_ns without progress
+    constexpr u64 kPrefetch = kToUser ? kPrefetchToUser : kPrefetchSlots;
+    constexpr u64 kFirst = kToUser ? kLookZeroCopy : kLookSend;   // loads the mover issues up front
+    Entries en;
+    en.init(len, S, (u64)GS, (u64)lane_id);
+    const volatile u64* loaded = &s_loaded;
+    u64 t0 = globaltimer();
+    unsigned it = 0;
+    for (u64 q = kFirst; q < en.total;) {
+      const u64 l = *loaded;
+      if (l == ~0ull) break;
+      if (q < l + kPrefetch) {
+        u64 ps, pe;
+        en.locate(q, &ps, &pe);
+        const Stripe& pst = en.stripe(ps);
+        const uint32_t nb = entry_bytes(pst, pe);
+        if (nb) bulk_prefetch_l2(p.src + lo + ps * S + pst.b0 + pe * kTmaChunk, nb);
+        ++q;
+        t0 = globaltimer();
+        continue;
+      }
+      if ((++it & 63u) == 0 && (op_aborted_device(w) || globaltimer() - t0 > w.timeout_ns)) break;
     }
   }
   if (discard && run && !sender && warp == 4) {

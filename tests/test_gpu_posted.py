@@ -121,11 +121,11 @@ def test_posted_operations_continue(env):
     xp.xp_fifo_destroy(fifo)
 
 
-@pytest.mark.parametrize("direct,lanes,rlanes,discard", [(False, 6, 7, False), (False, 10, 8, True),
-                                                       (True, 8, None, False)])
+@pytest.mark.parametrize("direct,lanes,rlanes,discard", [(False, 6, 7, False), (False, 9, 9, True),
+                                                       (True, 6, None, False), (True, 8, None, False)])
 def test_posted_workload(env, direct, lanes, rlanes, discard):
-    # 1 GiB of bf16 normals through 16 channels of 8 x 512 KiB; 10 + 8 lanes
-    # with discards on and direct at 8 lanes are the bench.py rows
+    # 1 GiB of bf16 normals through 16 channels of 8 x 512 KiB; 9 + 9 lanes
+    # with discards on and direct at 6 lanes are the bench.py rows
     torch, xp = env
     w = workloads.SIMPLE_MULTI
     src_np = workloads.normal_bf16_bits(w["nelems"], w["seed"]).view(np.uint8)
