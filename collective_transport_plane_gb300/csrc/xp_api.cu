@@ -143,6 +143,7 @@ xp_status mem_init(Mem& m, int nfifos) {
 
 struct Common {
   int device = 0;
+  unsigned long long ops = 0;    // operations launched: the id of the next one is ops + 1
   DevStatus* status = nullptr;   // device memory
   cudaEvent_t done = nullptr;
   cudaStream_t query = nullptr;
@@ -178,18 +179,23 @@ xp_status read_status(Common& c, int sync, xp_report* rep) {
   DevStatus h;
   XP_CUDA(cudaMemcpyAsync(&h, c.status, sizeof h, cudaMemcpyDeviceToHost, c.query));
   XP_CUDA(cudaStreamSynchronize(c.query));
+  // only the last operation's claim and occupancy count (their ids match
+  // the one the operation wrote as it started)
+  const unsigned long long id = h.last_op & 0xffffffffull;
+  const int code = (h.claim >> 32) == id ? (int)(uint32_t)h.claim : 0;
+  const uint32_t occupancy = (h.occupancy >> 32) == id ? (uint32_t)h.occupancy : 0u;
   if (rep) {
-    rep->code = h.code;
-    rep->channel = h.code ? h.channel : -1;
+    rep->code = code;
+    rep->channel = code ? h.channel : -1;
     rep->where = h.where;
     rep->reserved = 0;
     rep->observed = h.observed;
     rep->expected = h.expected;
-    rep->max_occupancy = h.max_occupancy;
+    rep->max_occupancy = occupancy;
     rep->reserved2 = 0;
   }
-  if (h.code < 0 || h.code > XP_ERR_INTERNAL) return XP_ERR_INTERNAL;
-  return static_cast<xp_status>(h.code);
+  if (code < 0 || code > XP_ERR_INTERNAL) return XP_ERR_INTERNAL;
+  return static_cast<xp_status>(code);
 }
 
 // Cluster co-residency: every cluster of the launch must fit on the GPU.
@@ -617,7 +623,7 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   if (launch_csize > xp::kMaxCluster)
     return fail(XP_ERR_INVALID, "%d channels x %d CTAs neither fit on the GPU at once nor form clusters of at most 16",
                 f->C, csize);
-  XP_CUDA(cudaMemsetAsync(f->cm.status, 0, xp::kStatusClearBytes, st));
+  p.op = ++f->cm.ops;
   const int grid = f->proto == XP_PROTO_SIMPLE ? f->C * csize : f->C * p.lanes * 2;
   if ((s = launch(kernel, grid, block, launch_csize, &p, st, smem)) != XP_OK) return s;
   if (mode == kOpProxy) xp::pump_kick(f->pump);
@@ -740,11 +746,12 @@ xp_status xp_ll_pingpong(xp_fifo* ab, xp_fifo* ba, int iters, uint64_t* elapsed_
   p.slot_bytes_ab = (unsigned)ab->S;
   p.slot_bytes_ba = (unsigned)ba->S;
   p.iters = iters;
-  p.elapsed = reinterpret_cast<unsigned long long*>(&ab->cm.status->pad1[0]);
+  p.elapsed = &ab->cm.status->elapsed;
   p.status = ab->cm.status;
   p.abort_word = g_abort_dev;
   p.timeout_ns = g_timeout_ns.load();
-  XP_CUDA(cudaMemsetAsync(ab->cm.status, 0, xp::kStatusClearBytes, st));
+  p.op = ++ab->cm.ops;
+  ++ba->cm.ops;
   if ((s = launch(xp::ll_pingpong_kernel_ptr(), 2, 32, 2, &p, st)) != XP_OK) return s;
   XP_CUDA(cudaEventRecord(ab->cm.done, st));
   XP_CUDA(cudaEventRecord(ba->cm.done, st));
@@ -752,8 +759,9 @@ xp_status xp_ll_pingpong(xp_fifo* ab, xp_fifo* ba, int iters, uint64_t* elapsed_
   XP_CUDA(cudaEventSynchronize(ab->cm.done));
   DevStatus h;
   XP_CUDA(cudaMemcpy(&h, ab->cm.status, sizeof h, cudaMemcpyDeviceToHost));
-  if (h.code != XP_OK) return static_cast<xp_status>(h.code);
-  *elapsed_ns = h.pad1[0];
+  if ((h.claim >> 32) == (p.op & 0xffffffffull) && (uint32_t)h.claim != XP_OK)
+    return static_cast<xp_status>((uint32_t)h.claim);
+  *elapsed_ns = h.elapsed;
   return XP_OK;
 }
 
@@ -850,7 +858,7 @@ xp_status xp_ring_allreduce_virtual(xp_ring* r, const void* const* send_bufs, vo
   p.status = r->cm.status;
   p.abort_word = g_abort_dev;
   p.timeout_ns = g_timeout_ns.load();
-  XP_CUDA(cudaMemsetAsync(r->cm.status, 0, xp::kStatusClearBytes, st));
+  p.op = ++r->cm.ops;
   if (r->place == XP_PLACE_DEVICE) {
     // HBM FIFOs: bulk copies through shared memory, every lane with its own
     // counters.  The ranks a lane's ring waits on must be resident together:

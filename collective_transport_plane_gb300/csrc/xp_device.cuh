@@ -116,17 +116,45 @@ struct WaitCtx {
   const volatile int* abort_word;
   u64 timeout_ns;
   int channel;
+  u64 op;
 };
 
+// The first failure of operation w.op claims the status block (a claim of
+// an earlier operation is replaced) and records where it happened.
 __device__ __forceinline__ void report(const WaitCtx& w, int code, int where, u64 observed, u64 expected) {
-  if (atomicCAS(&w.st->code, 0, code) == 0) {
-    w.st->channel = w.channel;
-    w.st->where = where;
-    w.st->observed = observed;
-    w.st->expected = expected;
+  const u64 mine = (w.op << 32) | (u64)(uint32_t)code;
+  u64 old = *reinterpret_cast<volatile u64*>(&w.st->claim);
+  for (;;) {
+    if ((old >> 32) == (w.op & 0xffffffffull) && (uint32_t)old != 0) break;   // already claimed
+    const u64 seen = atomicCAS(&w.st->claim, old, mine);
+    if (seen == old) {
+      w.st->channel = w.channel;
+      w.st->where = where;
+      w.st->observed = observed;
+      w.st->expected = expected;
+      break;
+    }
+    old = seen;
   }
   atomicExch(&w.st->sticky, 1);
   atomicExch(&w.st->abort, 1);
+}
+
+// At the start of an operation: the first CTA records the operation id, and
+// an object with a sticky failure refuses the operation (true).  One thread
+// per CTA.
+__device__ __forceinline__ bool op_begin(const WaitCtx& w) {
+  if (blockIdx.x == 0) *reinterpret_cast<volatile u64*>(&w.st->last_op) = w.op;
+  if (*reinterpret_cast<volatile int*>(&w.st->sticky)) {
+    report(w, XP_ERR_ABORTED, XP_WAIT_STICKY, 0, 0);
+    return true;
+  }
+  return false;
+}
+
+// Largest occupancy seen in operation `op` (the tag keeps older ones out).
+__device__ __forceinline__ void note_occupancy(DevStatus* st, u64 op, unsigned occ) {
+  atomicMax(&st->occupancy, (op << 32) | occ);
 }
 
 __device__ __forceinline__ bool op_aborted_device(const WaitCtx& w) {

@@ -56,23 +56,31 @@ constexpr int kP2pThreads = 32 * (kCopyWarps + 1);   // + 1 publisher warp
 constexpr int kRingThreads = 32 * (kCopyWarps + 2);  // + tail and head publishers
 constexpr int kLLThreads = 32 * (kCopyWarps + 1);
 
-// Device-side status of one operation (device memory).  The first 64 bytes
-// are cleared before every operation; `sticky` survives until a reset.
+// Device-side status of an object's operations (device memory).  Nothing
+// clears it between operations (a memset would be one more GPU operation per
+// call): every launch carries an operation id (the object's count of
+// launches) and the words an operation writes are tagged with it.  A failure
+// claims `claim` = (id << 32) | code unless this operation already holds it,
+// then fills channel, where, observed and expected, and sets `sticky` and
+// `abort`; while `sticky` is set (until a reset zeroes the block) every
+// operation is refused and claims ABORTED.  The host reports `claim` and the
+// occupancy word only when their id matches `last_op`, which the first CTA
+// of every operation writes as it starts.
 struct DevStatus {
-  int code;
+  unsigned long long claim;       // (op << 32) | code of the operation's first failure
   int channel;
   int where;
-  int abort;                      // set by the first failing wait: the others stop early
   unsigned long long observed;
   unsigned long long expected;
-  unsigned int max_occupancy;
+  unsigned long long occupancy;   // (op << 32) | largest tail - head a sender published in operation op
+  unsigned long long last_op;     // id of the last operation that started
+  int abort;                      // set by the first failing wait: the others stop early
   int pad0;
-  unsigned long long pad1[3];
+  unsigned long long elapsed;     // ping-pong: round-trip total, ns
   int sticky;                     // +64
   int pad2[15];
 };
 static_assert(sizeof(DevStatus) == 128, "status block layout");
-constexpr int kStatusClearBytes = 64;
 
 // Per-channel record of the last operation (device memory, one per channel),
 // written by the channel kernel: slot-steps moved, device time (globaltimer)
@@ -112,6 +120,7 @@ struct P2pParams {
   DevStatus* status;
   const volatile int* abort_word; // mapped host memory
   unsigned long long timeout_ns;
+  unsigned long long op;          // operation id (DevStatus)
 };
 
 struct PingParams {
@@ -128,6 +137,7 @@ struct PingParams {
   DevStatus* status;
   const volatile int* abort_word;
   unsigned long long timeout_ns;
+  unsigned long long op;
 };
 
 // Ring FIFOs keep kRingMaxLanes control blocks each: lane g of FIFO f (the
@@ -150,6 +160,7 @@ struct RingParams {
   DevStatus* status;
   const volatile int* abort_word;
   unsigned long long timeout_ns;
+  unsigned long long op;
 };
 
 }  // namespace xp

@@ -40,15 +40,11 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
   channel_range(p.nbytes, p.nchannels, ch, &lo, &hi);
   const u64 nlines = (hi - lo) / 8;
   const u64 nsteps = (nlines + L - 1) / L;
-  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch};
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch, p.op};
 
   if (threadIdx.x == 0) {
     s_base = ld_relaxed(basew);
-    s_stop = 0;
-    if (*reinterpret_cast<volatile int*>(&p.status->sticky)) {
-      s_stop = 1;
-      if (atomicCAS(&p.status->code, 0, XP_ERR_ABORTED) == 0) p.status->where = XP_WAIT_STICKY;
-    }
+    s_stop = op_begin(w) ? 1 : 0;
     if (!sender) {
       for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), kCopyWarps);
       mbar_init_fence();
@@ -157,9 +153,9 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
 // side is the receiver of one FIFO and returns its head for every line.
 __global__ void __launch_bounds__(32, 1) ll_pingpong_kernel(const PingParams p) {
   const unsigned crank = cluster_ctarank();
-  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, (int)crank};
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, (int)crank, p.op};
   cluster_sync_all();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && !op_begin(w)) {
     const bool is_a = crank == 0;
     char* sctl = is_a ? p.ctl_ab : p.ctl_ba;
     char* rctl = is_a ? p.ctl_ba : p.ctl_ab;

@@ -133,15 +133,11 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
   channel_range(p.nbytes, p.nchannels, ch, &lo, &hi);
   const u64 nwords = (hi - lo) / 8;
   const u64 nsteps = (nwords + W - 1) / W;
-  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch};
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch, p.op};
 
   if (threadIdx.x == 0) {
     s_base = ld_relaxed(basew);
-    s_stop = 0;
-    if (*reinterpret_cast<volatile int*>(&p.status->sticky)) {
-      s_stop = 1;
-      if (atomicCAS(&p.status->code, 0, XP_ERR_ABORTED) == 0) p.status->where = XP_WAIT_STICKY;
-    }
+    s_stop = op_begin(w) ? 1 : 0;
     if (!sender) {
       for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), kL128Warps);
       mbar_init_fence();

@@ -133,8 +133,10 @@ extern "C" xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t byt
   void* args[] = {&p};
   if ((e = cudaLaunchKernelExC(&cfg, xp::p2p_tma_kernel_ptr(0), args)) != cudaSuccess)
     return cuda_failed("cudaLaunchKernelExC", e);
+  // the claim word's low half is the failure code (the operation id, in the
+  // high half, is 0 here: the status block starts at zero on every call)
   if (dev_status &&
-      (e = cudaMemcpyAsync(dev_status, &status->code, sizeof(int32_t), cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
+      (e = cudaMemcpyAsync(dev_status, &status->claim, sizeof(int32_t), cudaMemcpyDeviceToDevice, st)) != cudaSuccess)
     return cuda_failed("cudaMemcpyAsync", e);
   return XP_OK;
 }

@@ -19,13 +19,7 @@
 namespace xp {
 
 __device__ __forceinline__ bool sticky_stop(const WaitCtx& w) {
-  if (*reinterpret_cast<volatile int*>(&w.st->sticky)) {
-    if (atomicCAS(&w.st->code, 0, XP_ERR_ABORTED) == 0) {
-      w.st->channel = w.channel;
-      w.st->where = XP_WAIT_STICKY;
-    }
-    return true;
-  }
+  if (op_begin(w)) return true;
   return false;
 }
 
@@ -60,7 +54,7 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
   channel_range(p.nbytes, p.nchannels, ch, &lo, &hi);
   const u64 len = hi - lo;
   const u64 nsteps = (len + S - 1) / S;
-  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch};
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch, p.op};
 
   if (threadIdx.x == 0) {
     s_base = ld_relaxed(basew);
@@ -172,7 +166,7 @@ __global__ void __launch_bounds__(kP2pThreads, 1) p2p_kernel(const P2pParams p) 
         }
       }
       if (sender) {
-        atomicMax(&p.status->max_occupancy, max_occ);
+        note_occupancy(p.status, p.op, max_occ);
         if (kZeroCopy && s == nsteps) {
           u64 hc = 0;
           if (wait_geq(head, base + nsteps, hc, w, XP_WAIT_HEAD)) st_release(ptrx, 0);

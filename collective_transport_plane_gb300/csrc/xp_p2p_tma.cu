@@ -233,19 +233,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   channel_range(p.nbytes, p.nchannels, ch, &lo, &hi);
   const u64 len = hi - lo;
   const u64 nsteps = (len + S - 1) / S;
-  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch};
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch, p.op};
   auto step_size = [&](u64 s) -> u64 { return (len - s * S) < S ? (len - s * S) : S; };
 
   if (threadIdx.x == 0) {
     s_base = ctl_relaxed<kProxy>(basew);
-    s_stop = 0;
-    if (*reinterpret_cast<volatile int*>(&p.status->sticky)) {
-      s_stop = 1;
-      if (atomicCAS(&p.status->code, 0, XP_ERR_ABORTED) == 0) {
-        p.status->channel = ch;
-        p.status->where = XP_WAIT_STICKY;
-      }
-    }
+    s_stop = op_begin(w) ? 1 : 0;
     s_mirror = 0;
     s_done = 0;
     s_read = 0;
@@ -311,7 +304,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         // take the completions in order and check the size each reports
         const u64 first = nsteps < N ? nsteps : N;
         for (u64 s = 0; s < first; ++s) post(s);
-        atomicMax(&p.status->max_occupancy, (unsigned)first);
+        note_occupancy(p.status, p.op, (unsigned)first);
         u64 j = 0;
         for (; j < nsteps; ++j) {
           const u64 k = (base + j) % N;
@@ -604,7 +597,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           ctl_release<kProxy>(head, step + 1);
         }
       }
-      if (sender != kPosted) atomicMax(&p.status->max_occupancy, max_occ);
+      if (sender != kPosted) note_occupancy(p.status, p.op, max_occ);
       if (sender) {
         if (kZeroCopy && s == nsteps) {
           u64 hc = 0;

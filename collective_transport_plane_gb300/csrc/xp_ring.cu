@@ -205,16 +205,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) ring_kernel(const RingParams 
   u64 clo, chi;
   ring_channel(p.count, align, p.nchannels, c, &clo, &chi);
   const u64 clen = chi - clo;
-  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, c * P + r};
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, c * P + r, p.op};
 
   if (threadIdx.x == 0) {
     s_rbase = ld_relaxed(base_recv);
     s_sbase = ld_relaxed(base_send);
-    s_stop = 0;
-    if (*reinterpret_cast<volatile int*>(&p.status->sticky)) {
-      s_stop = 1;
-      if (atomicCAS(&p.status->code, 0, XP_ERR_ABORTED) == 0) p.status->where = XP_WAIT_STICKY;
-    }
+    s_stop = op_begin(w) ? 1 : 0;
     if (leader_cta) {
       const uint32_t count = (uint32_t)(G * kCopyWarps);
       for (int k = 0; k < p.nslots; ++k) {
@@ -305,7 +301,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) ring_kernel(const RingParams 
         if (occ > max_occ) max_occ = (unsigned)occ;
       }
     }
-    if (pub_tail) atomicMax(&p.status->max_occupancy, max_occ);
+    if (pub_tail) note_occupancy(p.status, p.op, max_occ);
     if (!pub_tail && s == total) st_relaxed(base_recv, rbase + total);
   }
   __syncwarp();

@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kRThreads, 1) ring_tma_kernel(const RingParams
     chi = b < p.count ? b : p.count;
   }
   const u64 clen = chi - clo;
-  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, c * P + r};
+  const WaitCtx w{p.status, p.abort_word, p.timeout_ns, c * P + r, p.op};
 
   if (threadIdx.x == 0) {
     s_rbase = ld_relaxed(base_recv);
@@ -320,11 +320,7 @@ __global__ void __launch_bounds__(kRThreads, 1) ring_tma_kernel(const RingParams
     m_tail = 0;
     m_head = 0;
     s_done = 0;
-    s_stop = 0;
-    if (*reinterpret_cast<volatile int*>(&p.status->sticky)) {
-      s_stop = 1;
-      if (atomicCAS(&p.status->code, 0, XP_ERR_ABORTED) == 0) p.status->where = XP_WAIT_STICKY;
-    }
+    s_stop = op_begin(w) ? 1 : 0;
     for (int k = 0; k < kRStages; ++k) {
       mbar_init(smem_addr(&full[k]), 1);
       mbar_init(smem_addr(&computed[k]), 1);
@@ -566,7 +562,7 @@ __global__ void __launch_bounds__(kRThreads, 1) ring_tma_kernel(const RingParams
         }
         if (occ > max_occ) max_occ = (unsigned)occ;
       }
-      atomicMax(&p.status->max_occupancy, max_occ);
+      note_occupancy(p.status, p.op, max_occ);
     } else if (warp == 9 && lane == 0 && leader_cta) {
       // ---------------- head publisher (own FIFO) ----------------
       u64 s = 0;

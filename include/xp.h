@@ -29,9 +29,11 @@
  *     on its stream.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); every
  *     data-moving call is asynchronous on it and launches exactly one kernel
- *     after a small cudaMemsetAsync of the operation's status block
- *     (xp_send_recv_staged: one per chunk, plus its copies; xp_ll_pingpong is
- *     synchronous).
+ *     and nothing else (xp_send_recv_staged: one per chunk, plus its copies;
+ *     xp_send_recv_noalloc: one memset of its static FIFO's counters first;
+ *     xp_ll_pingpong is synchronous).  The status block is not cleared
+ *     between operations: each launch carries an operation id and the
+ *     status words a kernel writes are tagged with it.
  *   - Operations on one FIFO (or one ring) must be ordered: issue them on one
  *     stream, or synchronise between them.  Step counters live on the device
  *     and carry over from one operation to the next, so captured CUDA graphs
