@@ -21,6 +21,10 @@
 //               or the posts; receiver: tail, or the completions) and
 //               mirrors it into shared memory, so no copying thread stalls on
 //               a global-memory round trip;
+//   prefetcher - sender side: asks L2 to fetch src a bulk entry or two
+//               beyond the mover's loads (cp.async.bulk.prefetch);
+//   discarder - receiver side: drops the slot lines its stripe has read
+//               from L2;
 //   publisher - in the side's leader CTA only: waits until all lanes have
 //               signalled a slot-step on its arrival counter and publishes the one
 //               channel-wide counter (tail = step + 1 on the sender side,
