@@ -43,16 +43,22 @@ def test_wait_times_out_and_reports(env):
     assert st == xp.XP_ERR_TIMEOUT
     assert rep.where in (xp.XP_WAIT_HEAD, xp.XP_WAIT_TAIL, xp.XP_WAIT_SLOT_BARRIER)
     assert rep.channel == 0
-    # sticky: the next operation is refused on the device
-    xp.xp_send_recv(fifo, src, dst, 8192)
-    st, rep = xp.xp_fifo_status(fifo, True)
-    assert st == xp.XP_ERR_ABORTED and rep.where == xp.XP_WAIT_STICKY
-    # reset restores it
+    # sticky: the next operations are refused on the device, each claiming
+    # the status block for itself (the timeout's counters are not repeated)
+    for _ in range(2):
+        xp.xp_send_recv(fifo, src, dst, 8192)
+        st, rep = xp.xp_fifo_status(fifo, True)
+        assert st == xp.XP_ERR_ABORTED and rep.where == xp.XP_WAIT_STICKY
+        assert rep.observed == 0 and rep.expected == 0 and rep.channel == 0
+    # reset restores it; a good operation reports no failure and its own
+    # occupancy
     xp.xp_fifo_reset(fifo)
     xp.xp_set_spin_timeout_ns(2_000_000_000)
-    xp.xp_send_recv(fifo, src, dst, 8192)
-    st, _ = xp.xp_fifo_status(fifo, True)
-    assert st == xp.XP_OK and bool((dst == 1).all())
+    for _ in range(2):
+        xp.xp_send_recv(fifo, src, dst, 8192)
+        st, rep = xp.xp_fifo_status(fifo, True)
+        assert st == xp.XP_OK and bool((dst == 1).all())
+        assert rep.channel == -1 and 1 <= rep.max_occupancy <= 2
     xp.xp_fifo_destroy(fifo)
 
 

@@ -77,6 +77,11 @@ def test_p2p_graph_replay(env, mode):
         torch.cuda.synchronize()
         st, rep = xp.xp_fifo_status(fifo, True)
         assert st == xp.XP_OK, (st, rep.where, rep.observed, rep.expected)
+        assert rep.channel == -1
+        if mode in ("simple", "zero_copy", "ce", "posted_direct"):
+            # the replay's own occupancy: status words carry the captured
+            # operation's id, which the replay also writes as it starts
+            assert 1 <= rep.max_occupancy <= nslots
         assert np.array_equal(from_dev(dst), want)
     xp.xp_fifo_destroy(fifo)
 
@@ -95,7 +100,8 @@ def test_ring_graph_replay(env):
             t.copy_(torch.from_numpy(x))
         g.replay()
         torch.cuda.synchronize()
-        assert xp.xp_ring_status(ring, True)[0] == xp.XP_OK
+        st, rep = xp.xp_ring_status(ring, True)
+        assert st == xp.XP_OK and 1 <= rep.max_occupancy <= nslots
         for t in outs:
             assert np.array_equal(from_dev(t), want)
     xp.xp_ring_destroy(ring)
