@@ -124,7 +124,12 @@ void mem_free(Mem& m) {
 
 // Zero the whole region, then set every size word of `nfifos` control
 // blocks to -1.
-xp_status mem_init(Mem& m, int nfifos) {
+// Set-up and reset write device memory on the object's own non-blocking
+// stream (`st`) and wait for that stream only.  A copy on the legacy default
+// stream would queue behind whatever runs there, such as a proxy-mode
+// transfer that waits for the pump's copies, and could hold those copies up
+// in a shared copy queue until the transfer times out.
+xp_status mem_init(Mem& m, int nfifos, cudaStream_t st) {
   const size_t ctl_bytes = (size_t)nfifos * xp::kCtlBytes;
   std::vector<char> img(ctl_bytes, 0);
   for (int f = 0; f < nfifos; ++f) {
@@ -132,8 +137,9 @@ xp_status mem_init(Mem& m, int nfifos) {
     for (int k = 0; k < xp::kMaxSlots; ++k) sz[k] = -1;
   }
   if (m.place == XP_PLACE_DEVICE) {
-    XP_CUDA(cudaMemset(m.dev, 0, m.bytes));
-    XP_CUDA(cudaMemcpy(m.dev, img.data(), ctl_bytes, cudaMemcpyHostToDevice));
+    XP_CUDA(cudaMemsetAsync(m.dev, 0, m.bytes, st));
+    XP_CUDA(cudaMemcpyAsync(m.dev, img.data(), ctl_bytes, cudaMemcpyHostToDevice, st));
+    XP_CUDA(cudaStreamSynchronize(st));
   } else {
     memset(m.host, 0, m.bytes);
     memcpy(m.host, img.data(), ctl_bytes);
@@ -153,9 +159,10 @@ struct Common {
 xp_status common_init(Common& c) {
   XP_CUDA(cudaGetDevice(&c.device));
   XP_CUDA(cudaMalloc(reinterpret_cast<void**>(&c.status), sizeof(DevStatus)));
-  XP_CUDA(cudaMemset(c.status, 0, sizeof(DevStatus)));
   XP_CUDA(cudaEventCreateWithFlags(&c.done, cudaEventDisableTiming));
   XP_CUDA(cudaStreamCreateWithFlags(&c.query, cudaStreamNonBlocking));
+  XP_CUDA(cudaMemsetAsync(c.status, 0, sizeof(DevStatus), c.query));
+  XP_CUDA(cudaStreamSynchronize(c.query));
   return XP_OK;
 }
 
@@ -407,16 +414,17 @@ xp_status xp_fifo_create(int nchannels, int nslots, size_t slot_bytes, xp_proto 
   f->ch_stride = round_up((size_t)nslots * slot_bytes, 4096);
   if ((s = common_init(f->cm)) != XP_OK ||
       (s = mem_alloc(f->mem, f->ctl_region + f->pctl_region + nchannels * f->ch_stride, place)) != XP_OK ||
-      (s = mem_init(f->mem, nchannels)) != XP_OK) {
+      (s = mem_init(f->mem, nchannels, f->cm.query)) != XP_OK) {
     common_free(f->cm);
     mem_free(f->mem);
     delete f;
     return s;
   }
   if (cudaMalloc(reinterpret_cast<void**>(&f->stats), (size_t)nchannels * sizeof(xp::ChanStats)) != cudaSuccess ||
-      cudaMemset(f->stats, 0, (size_t)nchannels * sizeof(xp::ChanStats)) != cudaSuccess ||
+      cudaMemsetAsync(f->stats, 0, (size_t)nchannels * sizeof(xp::ChanStats), f->cm.query) != cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&f->arr), (size_t)nchannels * xp::kArrBytes) != cudaSuccess ||
-      cudaMemset(f->arr, 0, (size_t)nchannels * xp::kArrBytes) != cudaSuccess) {
+      cudaMemsetAsync(f->arr, 0, (size_t)nchannels * xp::kArrBytes, f->cm.query) != cudaSuccess ||
+      cudaStreamSynchronize(f->cm.query) != cudaSuccess) {
     if (f->stats) cudaFree(f->stats);
     if (f->arr) cudaFree(f->arr);
     common_free(f->cm);
@@ -713,8 +721,9 @@ xp_status xp_fifo_stats(xp_fifo* f, int channel, xp_channel_stats* out) {
 xp_status xp_fifo_reset(xp_fifo* f) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (f->cm.used) XP_CUDA(cudaEventSynchronize(f->cm.done));
-  XP_CUDA(cudaMemset(f->cm.status, 0, sizeof(DevStatus)));
-  XP_CUDA(cudaMemset(f->arr, 0, (size_t)f->C * xp::kArrBytes));
+  XP_CUDA(cudaMemsetAsync(f->cm.status, 0, sizeof(DevStatus), f->cm.query));
+  XP_CUDA(cudaMemsetAsync(f->arr, 0, (size_t)f->C * xp::kArrBytes, f->cm.query));
+  XP_CUDA(cudaStreamSynchronize(f->cm.query));
   if (f->pump) {
     // restart the pump on zeroed proxy counters
     xp::pump_stop(f->pump);
@@ -724,7 +733,7 @@ xp_status xp_fifo_reset(xp_fifo* f) {
     f->pump = xp::pump_start(pump_config(f), &err);
     if (!f->pump) return fail(XP_ERR_CUDA, "%s", err.c_str());
   }
-  return mem_init(f->mem, f->C);
+  return mem_init(f->mem, f->C, f->cm.query);
 }
 
 xp_status xp_ll_pingpong(xp_fifo* ab, xp_fifo* ba, int iters, uint64_t* elapsed_ns, xp_stream_t stream) {
@@ -758,7 +767,8 @@ xp_status xp_ll_pingpong(xp_fifo* ab, xp_fifo* ba, int iters, uint64_t* elapsed_
   ab->cm.used = ba->cm.used = true;
   XP_CUDA(cudaEventSynchronize(ab->cm.done));
   DevStatus h;
-  XP_CUDA(cudaMemcpy(&h, ab->cm.status, sizeof h, cudaMemcpyDeviceToHost));
+  XP_CUDA(cudaMemcpyAsync(&h, ab->cm.status, sizeof h, cudaMemcpyDeviceToHost, ab->cm.query));
+  XP_CUDA(cudaStreamSynchronize(ab->cm.query));
   if ((h.claim >> 32) == (p.op & 0xffffffffull) && (uint32_t)h.claim != XP_OK)
     return static_cast<xp_status>((uint32_t)h.claim);
   *elapsed_ns = h.elapsed;
@@ -786,7 +796,7 @@ xp_status xp_ring_create(int nranks, int nchannels, int nslots, size_t slot_byte
   r->ctl_region = round_up((size_t)nf * xp::kRingMaxLanes * xp::kCtlBytes, 4096);
   r->fifo_stride = round_up((size_t)nslots * slot_bytes, 4096);
   if ((s = common_init(r->cm)) != XP_OK || (s = mem_alloc(r->mem, r->ctl_region + nf * r->fifo_stride, place)) != XP_OK ||
-      (s = mem_init(r->mem, nf * xp::kRingMaxLanes)) != XP_OK) {
+      (s = mem_init(r->mem, nf * xp::kRingMaxLanes, r->cm.query)) != XP_OK) {
     common_free(r->cm);
     mem_free(r->mem);
     delete r;
@@ -885,8 +895,8 @@ xp_status xp_ring_status(xp_ring* r, int sync, xp_report* report) {
 xp_status xp_ring_reset(xp_ring* r) {
   if (!r) return fail(XP_ERR_INVALID, "ring is NULL");
   if (r->cm.used) XP_CUDA(cudaEventSynchronize(r->cm.done));
-  XP_CUDA(cudaMemset(r->cm.status, 0, sizeof(DevStatus)));
-  return mem_init(r->mem, r->P * r->C);
+  XP_CUDA(cudaMemsetAsync(r->cm.status, 0, sizeof(DevStatus), r->cm.query));
+  return mem_init(r->mem, r->P * r->C * xp::kRingMaxLanes, r->cm.query);
 }
 
 }  // extern "C"

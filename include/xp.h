@@ -272,7 +272,13 @@ xp_status xp_fifo_enable_ce(xp_fifo* f);
  * xp_fifo_status leaves the pump's message in xp_last_error()).  The pump
  * keeps serving while the FIFO exists, so captured graphs replay.  Proxy
  * operations keep their own counters; other operations may alternate with
- * them on the FIFO. */
+ * them on the FIFO.  The transfer's kernel waits for the pump's copies, so
+ * while it is in flight the process should not queue copies that wait for
+ * it (for example a cudaMemcpy on the stream it runs on, or on the legacy
+ * default stream when it runs there): such a copy can share a copy queue
+ * with the pump's and hold them up until the transfer stops at its spin
+ * timeout.  This library's own set-up calls never do (they use streams of
+ * their own), so objects may be created, reset or destroyed meanwhile. */
 xp_status xp_send_recv_ce(xp_fifo* f, const void* src, void* dst, size_t bytes, xp_stream_t stream);
 
 /* xp_send_recv from host memory to host memory, staged through device

@@ -186,3 +186,28 @@ def test_pump_refuses_a_bad_size_word(env):
     finally:
         xp.xp_set_spin_timeout_ns(2_000_000_000)
     xp.xp_fifo_destroy(f)
+
+
+def test_objects_created_while_a_proxy_transfer_runs(env):
+    # FIFOs and rings are set up on streams of their own, so creating,
+    # resetting and destroying them while a proxy transfer waits for the
+    # pump's copies neither waits for that transfer nor holds the copies up
+    torch, xp = env
+    xp.xp_set_spin_timeout_ns(500_000_000)
+    try:
+        f = _fifo(xp, 2, 4, 65536, 0)
+        src = to_dev(torch, workloads.uniform_bytes(1 << 20, seed=21))
+        dst = torch.zeros_like(src)
+        for make in (lambda: xp.xp_fifo_destroy(xp.xp_fifo_create(2, 2, 4096)),
+                     lambda: xp.xp_ring_destroy(xp.xp_ring_create(4, 2, 4, 65536)),
+                     lambda: xp.xp_fifo_destroy(xp.xp_fifo_create(2, 2, 4096, xp.XP_PROTO_LL128))):
+            dst.zero_()
+            torch.cuda.synchronize()
+            xp.xp_send_recv_ce(f, src, dst, 1 << 20, torch.cuda.current_stream())
+            make()
+            st, rep = xp.xp_fifo_status(f, True)
+            assert st == xp.XP_OK, (st, rep.where)
+            assert torch.equal(src, dst)
+        xp.xp_fifo_destroy(f)
+    finally:
+        xp.xp_set_spin_timeout_ns(2_000_000_000)
