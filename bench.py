@@ -375,7 +375,7 @@ def main():
     return 0
 
 
-def e2e_row(torch, xp, fifo, src_np, stream, iters=5, chunk=64 << 20):
+def e2e_row(torch, xp, fifo, src_np, stream, iters=10, warmup=3, chunk=64 << 20):
     """Same transfer from pinned host memory to pinned host memory through the
     C ABI (xp_send_recv_staged): host -> device copies, the FIFO transfers and
     device -> host copies of 64 MiB chunks, overlapped on three streams, all
@@ -390,14 +390,16 @@ def e2e_row(torch, xp, fifo, src_np, stream, iters=5, chunk=64 << 20):
         xp.xp_send_recv_staged(fifo, h_src, h_dst, d_src, d_dst, n, chunk, stream)
 
     with torch.cuda.stream(stream):
-        one()
+        for _ in range(warmup):
+            one()
         torch.cuda.synchronize()
         t = time_events(torch, stream, one, iters)
     if not torch.equal(h_dst, h_src):
         raise RuntimeError("end-to-end transfer is not byte-exact")
     ms = sum(t) / iters
     return {"value": n / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": n, "d2h_bytes_per_step": n,
-            "ms_per_step": ms, "api": "xp_send_recv_staged", "chunk_bytes": chunk}
+            "ms_per_step": ms, "ms_min": min(t), "ms_max": max(t), "steps": iters, "warmup": warmup,
+            "api": "xp_send_recv_staged", "chunk_bytes": chunk}
 
 
 ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "ce", "loopback", "ll", "ll128", "host_fifo", "ring")
