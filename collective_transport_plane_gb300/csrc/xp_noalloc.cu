@@ -39,7 +39,7 @@ constexpr unsigned long long kNoallocTimeoutNs = 2000000000ull;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
 std::mutex g_noalloc_mu;
-unsigned char* g_noalloc_dev[64] = {};   // device address of the array, per device
+bool g_noalloc_ready[64] = {};   // per device: the kernel's shared-memory attribute is set
 
 size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
@@ -78,20 +78,22 @@ extern "C" xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t byt
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_failed("cudaGetDevice", e);
   if (dev < 0 || dev >= 64) return invalid("xp_send_recv_noalloc: device index above 63");
-  unsigned char* base = nullptr;
+  // The array's device address, looked up on every call with this device
+  // current (the lookup allocates nothing, and a context created anew, say
+  // after cudaDeviceReset, maps the array at a new address).
+  void* ptr = nullptr;
+  if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess) return cuda_failed("cudaGetSymbolAddress", e);
+  if (!ptr) return invalid("xp_send_recv_noalloc: no device address for the static FIFO");
+  unsigned char* base = static_cast<unsigned char*>(ptr);
   {
-    // once per device, with that device current: the array's device address
+    // once per device: let the kernel use its dynamic shared memory
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_dev[dev]) {
-      void* ptr = nullptr;
-      if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess) return cuda_failed("cudaGetSymbolAddress", e);
-      if (!ptr) return invalid("xp_send_recv_noalloc: no device address for the static FIFO");
+    if (!g_noalloc_ready[dev]) {
       const void* kern = xp::p2p_tma_kernel_ptr(0);
       if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, xp::p2p_tma_smem())) != cudaSuccess)
         return cuda_failed("cudaFuncSetAttribute", e);
-      g_noalloc_dev[dev] = static_cast<unsigned char*>(ptr);
+      g_noalloc_ready[dev] = true;
     }
-    base = g_noalloc_dev[dev];
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   xp::DevStatus* status = reinterpret_cast<xp::DevStatus*>(base + kNoallocStatusOff);

@@ -387,8 +387,9 @@ xp_status xp_ring_reset(xp_ring* r);
  * not NULL, copies the device-side xp_status of the transfer there
  * asynchronously.  All calls share the one array: calls whose transfers
  * overlap in time on the GPU (other streams, other host threads) race and
- * corrupt each other.  The first call on a device looks up the array's
- * device address and sets a kernel attribute; make it before any stream
+ * corrupt each other.  Every call looks up the array's device address
+ * (cudaGetSymbolAddress, with the caller's device current); the first call
+ * on a device also sets a kernel attribute, so make it before any stream
  * capture.  Nothing here calls cudaMalloc, cudaFree or an allocating
  * library routine. */
 xp_status xp_send_recv_noalloc(const void* src, void* dst, size_t bytes, int nchannels, int nslots,
