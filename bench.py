@@ -425,7 +425,8 @@ def e2e_row(torch, xp, fifo, src_np, stream, iters=10, warmup=3, chunk=64 << 20)
             "api": "xp_send_recv_staged", "chunk_bytes": chunk}
 
 
-ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "ce", "loopback", "ll", "ll128", "host_fifo", "ring")
+ROW_GROUPS = ("hbm", "zero_copy", "simple_lanes1", "posted", "ce", "loopback", "ll", "ll128", "host_fifo", "ce_host",
+              "ring")
 
 
 def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
@@ -653,6 +654,15 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         ceiling = n / (best * 1e-3) / 1e9
         top = max(v["gbs"] for v in host.values())
         res["host_fifo"] = {"by_lanes": host, "ceiling_concurrent_memcpy_gbs": ceiling, "frac_of_ceiling": top / ceiling}
+        del hp, hq, d1, d2
+
+    if want("ce_host"):
+        wh = workloads.HOST_FIFO
+        if not want("host_fifo"):
+            src = torch.from_numpy(workloads.uniform_f32(wh["nelems"], wh["seed"])).to("cuda")
+            dst = torch.empty_like(src)
+            n = src.numel() * 4
+            ceiling = None
         # the same FIFO in proxy mode (shm useMemcpy style): the pump's copy
         # engines move each slot-step device -> host FIFO -> device
         f = xp.xp_fifo_create(wh["nchannels"], wh["nslots"], wh["slot_bytes"], xp.XP_PROTO_SIMPLE,
@@ -666,10 +676,13 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
             t = time_events(torch, s, lambda: xp.xp_send_recv_ce(f, src, dst, n, s), 10)
         st, _ = xp.xp_fifo_status(f, True)
         ms = statistics.median(t)
-        res["ce_host_2hops"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "ms_best": min(t), "ms_median": ms, "frac_of_ceiling": n / (ms * 1e-3) / 1e9 / ceiling,
+        res["ce_host_2hops"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "ms_best": min(t), "ms_median": ms,
+                                "frac_of_ceiling": n / (ms * 1e-3) / 1e9 / ceiling if ceiling else None,
                                 "exact": bool(st == 0 and torch.equal(dst, src))}
         xp.xp_fifo_destroy(f)
-        del src, dst, hp, hq, d1, d2
+
+    if want("host_fifo") or want("ce_host"):
+        del src, dst
 
     if want("ring"):
         # virtual ring allreduce: 8 ranks x 256 MiB fp32, 8 channels x 8 x 512 KiB
