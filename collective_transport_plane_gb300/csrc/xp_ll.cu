@@ -43,14 +43,18 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
   const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch, p.op};
 
   if (threadIdx.x == 0) {
-    s_base = ld_relaxed(basew);
+    const u64 b0 = ld_relaxed(basew);   // in flight while op_begin reads the sticky word
     s_stop = op_begin(w) ? 1 : 0;
+    s_base = b0;
     if (!sender) {
       for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), kCopyWarps);
       mbar_init_fence();
     }
   }
-  cluster_sync_all();
+  // The two CTAs of the cluster share no shared memory (each side's barriers
+  // are its own), so a block barrier is enough here and none is needed at
+  // the end; the cluster launch still schedules sender and receiver together.
+  __syncthreads();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
   ChanStats* cs = p.stats ? p.stats + ch : nullptr;
@@ -144,8 +148,6 @@ __global__ void __launch_bounds__(kLLThreads, 1) ll_kernel(const P2pParams p) {
     if (r == nsteps) st_relaxed(basew, base + nsteps);
     if (cs) cs->t_end = globaltimer();
   }
-  __syncwarp();
-  cluster_sync_all();
 }
 
 // Ping-pong: CTA 0 (A) sends one line through `ab`, CTA 1 (B) answers

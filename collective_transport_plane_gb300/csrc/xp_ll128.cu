@@ -136,8 +136,9 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
   const WaitCtx w{p.status, p.abort_word, p.timeout_ns, ch, p.op};
 
   if (threadIdx.x == 0) {
-    s_base = ld_relaxed(basew);
+    const u64 b0 = ld_relaxed(basew);   // in flight while op_begin reads the sticky word
     s_stop = op_begin(w) ? 1 : 0;
+    s_base = b0;
     if (!sender) {
       for (int k = 0; k < p.nslots; ++k) mbar_init(smem_addr(&bars[k]), kL128Warps);
       mbar_init_fence();
@@ -150,7 +151,10 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
       mbar_init_fence();
     }
   }
-  cluster_sync_all();
+  // Each CTA's barriers are its own (no shared memory is used across the
+  // pair), so a block barrier is enough here and none is needed at the end;
+  // the cluster launch still schedules the pair together.
+  __syncthreads();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
   ChanStats* cs = p.stats ? p.stats + ch : nullptr;
@@ -422,8 +426,6 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
       }
     }
   }
-  __syncwarp();
-  cluster_sync_all();
 }
 
 void* ll128_kernel_ptr() { return reinterpret_cast<void*>(&ll128_kernel); }

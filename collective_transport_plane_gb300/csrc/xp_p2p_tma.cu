@@ -241,8 +241,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   auto step_size = [&](u64 s) -> u64 { return (len - s * S) < S ? (len - s * S) : S; };
 
   if (threadIdx.x == 0) {
-    s_base = ctl_relaxed<kProxy>(basew);
+    const u64 b0 = ctl_relaxed<kProxy>(basew);   // in flight while op_begin reads the sticky word
     s_stop = op_begin(w) ? 1 : 0;
+    s_base = b0;
     s_mirror = 0;
     s_done = 0;
     s_read = 0;
