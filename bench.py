@@ -57,27 +57,28 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES, root: str = ROOT) -> str:
     """Hash of a kernel's sources with comments and whitespace removed, so that
     only a change of code makes a committed ncu capture stale."""
     h = hashlib.sha256()
     for f in sources:
-        src = open(os.path.join(ROOT, "collective_transport_plane_gb300", "csrc", f)).read()
+        src = open(os.path.join(root, "collective_transport_plane_gb300", "csrc", f)).read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
         src = re.sub(r"//[^\n]*", " ", src)
         h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name: str = "p2p_tma_simple_1GiB_16ch"):
+def profiled_traffic(name: str = "p2p_tma_simple_1GiB_16ch", root: str = ROOT):
     """DRAM bytes per launch of a kernel from its committed ncu record
     (profiles/<name>.json), if the kernel's sources have not changed since it
     was captured; else None."""
     try:
-        rec = json.load(open(os.path.join(ROOT, "profiles", name + ".json")))
+        rec = json.load(open(os.path.join(root, "profiles", name + ".json")))
+        current = kernel_source_hash(rec.get("sources", KERNEL_SOURCES), root)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_source_hash") != kernel_source_hash(rec.get("sources", KERNEL_SOURCES)):
+    if rec.get("kernel_source_hash") != current:
         return None
     return int(rec["traffic_bytes_per_launch"])
 
