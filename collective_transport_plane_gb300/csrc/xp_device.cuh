@@ -423,6 +423,12 @@ static __device__ __noinline__ bool wait_mirror(const u64* m, u64 target, u64& c
   }
 }
 
+// Everything this thread has done or observed in memory is performed at GPU
+// scope before anything it does next.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // Order this thread's async-proxy (bulk copy) accesses of global memory with
 // its generic-proxy accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

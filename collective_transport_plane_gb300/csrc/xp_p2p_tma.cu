@@ -29,7 +29,9 @@
 //               signalled a slot-step on its arrival counter and publishes the one
 //               channel-wide counter (tail = step + 1 on the sender side,
 //               head = step + 1 on the receiver side; posted modes: the
-//               completion, or the next post).
+//               completion, or the next post).  A side of one lane has
+//               nothing to aggregate: its publisher takes the signals from
+//               shared memory, a global-memory round trip shorter.
 // A sender stripe is signalled once its bulk stores have completed.  The mover
 // checks that only after the first store of the next step is in flight, so the
 // store pipeline never drains at a step boundary, and before it blocks on
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   __shared__ u64 s_mirror;   // latest head / post (sender) or tail / completion (receiver) seen by the watcher
   __shared__ u64 s_done;     // sender: steps [0, s_done) have their bulk stores complete
   __shared__ u64 s_read;     // receiver: steps [0, s_read) have their slot stripe in shared memory
+  __shared__ u64 s_freed;    // receiver of one lane: steps [0, s_freed) may be refilled
   __shared__ u64 s_loaded;   // sender: bulk loads the mover has issued (~0: the mover is done)
   __shared__ u64 s_addr[kPosted ? kMaxSlots : 1];   // posted sender: address and size of each slot's post
   __shared__ u64 s_cap[kPosted ? kMaxSlots : 1];
@@ -247,6 +250,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
     s_mirror = 0;
     s_done = 0;
     s_read = 0;
+    s_freed = 0;
     s_loaded = 0;
     for (int k = 0; k < kTmaStages; ++k) {
       mbar_init(smem_addr(&full[k]), 1);
@@ -474,7 +478,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       // thread's own memory traffic; this thread has none in flight, the
       // mover always has.
       u64 done = 0;
-      for (u64 s = 0; s < nsteps; ++s) {
+      for (u64 s = 0; s < nsteps && GS > 1; ++s) {   // one lane: the publisher reads s_done itself
         if (!wait_mirror(&s_done, s + 1, done, w, XP_WAIT_SLOT_BARRIER)) break;
         red_add_release(arrivals + (base + s) % N, 1);
       }
@@ -497,8 +501,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
           if (e + 1 == st.nent) {
             if (discard)
               st_release_cta_shared(&s_read, s + 1);   // the discarder returns the credit
-            else
+            else if (GS > 1)
               red_add_relaxed(arrivals + (base + s) % N, 1);
+            else
+              st_release_cta_shared(&s_freed, s + 1);
           }
           const uint32_t nb = entry_bytes(st, e);
           if (nb) bulk_store(p.dst + lo + s * S + st.b0 + e * kTmaChunk, sm0 + k * kTmaChunk, nb, pol_user);
@@ -575,9 +581,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
         for (u64 q = 0; q < first; ++q) post(q);
         max_occ = (unsigned)first;
       }
+      u64 mine = 0;
       for (; s < nsteps; ++s) {
         const u64 step = base + s;
-        {
+        if (GS == 1) {
+          if (!wait_mirror(sender ? &s_done : &s_freed, s + 1, mine, w, XP_WAIT_SLOT_BARRIER)) break;
+        } else {
           u64 c = 0;
           if (!wait_geq(arrivals + step % N, (u64)GS, c, w, XP_WAIT_SLOT_BARRIER)) break;
           red_add_relaxed(arrivals + step % N, 0ull - (u64)GS);
@@ -647,7 +656,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
     // ---------------- discarder ----------------
     // once the storer has seen a step's stripe land in shared memory, drop
     // the 128-byte lines lying wholly inside the stripe from L2 (lines shared
-    // with a neighbouring lane's stripe stay), then signal the slot consumed
+    // with a neighbouring lane's stripe stay), then signal the slot consumed:
+    // with a release, so the drops are performed before the sender may
+    // refill the slot.  The operation's last step is signalled first and its
+    // lines dropped after: nothing refills that slot before the kernel has
+    // ended, so its credit need not wait for the drops.
     Entries en;
     en.init(len, S, (u64)GS, (u64)lane_id);
     u64 seen = 0;
@@ -655,13 +668,26 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
       int ok = 1;
       if (lane == 0) ok = wait_mirror(&s_read, s + 1, seen, w, XP_WAIT_SLOT_BARRIER) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const bool last = s + 1 == nsteps;
+      if (last && lane == 0) {
+        // the stripe's reads are complete: the signal carries no ordering
+        if (GS > 1) red_add_relaxed(arrivals + (base + s) % N, 1);
+        else st_release_cta_shared(&s_freed, s + 1);
+      }
       const Stripe& st = en.stripe(s);
       const u64 from = reinterpret_cast<u64>(slots_recv + ((base + s) % N) * S);
       const u64 l0 = (from + st.b0 + 127) & ~127ull;
       const u64 l1 = (from + st.b0 + st.fb + st.rag) & ~127ull;
       for (u64 x = l0 + 128ull * lane; x < l1; x += 128ull * 32) discard_l2(reinterpret_cast<void*>(x));
       __syncwarp();
-      if (lane == 0) red_add_release(arrivals + (base + s) % N, 1);
+      if (!last && lane == 0) {
+        if (GS > 1) {
+          red_add_release(arrivals + (base + s) % N, 1);
+        } else {
+          fence_acq_rel_gpu();   // the warp's drops performed, then the publisher may return the credit
+          st_release_cta_shared(&s_freed, s + 1);
+        }
+      }
     }
   }
   __syncwarp();

@@ -18,6 +18,7 @@ XP_OK, XP_ERR_INVALID, XP_ERR_CUDA, XP_ERR_TIMEOUT, XP_ERR_BOUNDS, XP_ERR_ABORTE
 XP_PROTO_SIMPLE, XP_PROTO_LL, XP_PROTO_LL128 = 0, 1, 2
 XP_PLACE_DEVICE, XP_PLACE_HOST_MAPPED = 0, 1
 XP_U8, XP_U32, XP_I32, XP_F32, XP_BF16 = range(5)
+XP_DISCARD_AUTO_BYTES = 48 << 20   # include/xp.h: FIFOs at least this large drop read slot lines by default
 (XP_WAIT_NONE, XP_WAIT_HEAD, XP_WAIT_TAIL, XP_WAIT_PTR_EXCHANGE, XP_WAIT_LL_FLAG, XP_WAIT_SLOT_BARRIER,
  XP_WAIT_SIZE_WORD, XP_WAIT_OCCUPANCY, XP_WAIT_STICKY, XP_WAIT_POST, XP_WAIT_COMPLETION) = range(11)
 
@@ -42,7 +43,8 @@ class xp_channel_desc(ctypes.Structure):
     _fields_ = [("ctl", ctypes.c_void_p), ("slots", ctypes.c_void_p), ("slot_stride", ctypes.c_size_t),
                 ("nslots", ctypes.c_int), ("proto", ctypes.c_int), ("placement", ctypes.c_int),
                 ("lanes", ctypes.c_int), ("recv_lanes", ctypes.c_int), ("posted", ctypes.c_void_p),
-                ("ce", ctypes.c_void_p), ("send_ring", ctypes.c_void_p), ("recv_ring", ctypes.c_void_p)]
+                ("ce", ctypes.c_void_p), ("send_ring", ctypes.c_void_p), ("recv_ring", ctypes.c_void_p),
+                ("discard", ctypes.c_int)]
 
 
 class xp_channel_stats(ctypes.Structure):
@@ -176,8 +178,9 @@ def xp_fifo_stats(fifo: int, channel: int) -> xp_channel_stats:
     return out
 
 
-def xp_fifo_set_discard(fifo: int, on: bool) -> None:
-    _check(_lib.xp_fifo_set_discard(fifo, 1 if on else 0), "xp_fifo_set_discard")
+def xp_fifo_set_discard(fifo: int, on: bool | None) -> None:
+    """True: drop read slot lines; False: keep them; None: choose by the FIFO's size."""
+    _check(_lib.xp_fifo_set_discard(fifo, -1 if on is None else (1 if on else 0)), "xp_fifo_set_discard")
 
 
 def xp_fifo_enable_ce(fifo: int) -> None:

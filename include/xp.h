@@ -136,6 +136,7 @@ typedef struct {
   void* ce;
   void* send_ring;
   void* recv_ring;
+  int discard;        /* 1: the next operation's receivers drop the slot lines they read (xp_fifo_set_discard) */
 } xp_channel_desc;
 
 /* Create a FIFO of `nchannels` independent channels, each with `nslots`
@@ -182,13 +183,19 @@ xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
 xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes);
 
 /* Whether receivers that read FIFO slots in HBM drop each 128-byte line of
- * their stripe from L2 (discard.global.L2) once they have read it, before
- * returning credit (on != 0, the default) — the data is dead, and this saves
- * writing it back to DRAM — or leave it (on == 0).  With it on, the slots'
- * bytes after a transfer are undefined; with it off they hold the last
- * slot-steps that passed through, as in the pages' protocol.  Applies to
- * xp_send_recv, copy-mode xp_send_recv_posted and xp_send_recv_ce on HBM
- * FIFOs; takes effect at the next operation. */
+ * their stripe from L2 (discard.global.L2) once they have read it — the data
+ * is dead, and this saves writing it back to DRAM when L2 would evict it
+ * before the slot is refilled — (on > 0), leave it (on == 0), or choose by
+ * the FIFO's size (on < 0, the default): drop when nchannels * nslots *
+ * slot_bytes >= XP_DISCARD_AUTO_BYTES, whose lines compete for L2 with the
+ * user buffers streaming through; a smaller FIFO's lines are rewritten
+ * before eviction, and the drops would only delay its credit.  With drops on,
+ * the slots' bytes after a transfer are undefined; with them off they hold
+ * the last slot-steps that passed through, as in the pages' protocol.
+ * Applies to xp_send_recv, copy-mode xp_send_recv_posted and xp_send_recv_ce
+ * on HBM FIFOs; takes effect at the next operation; xp_fifo_describe reports
+ * the choice. */
+#define XP_DISCARD_AUTO_BYTES ((size_t)48 << 20)
 xp_status xp_fifo_set_discard(xp_fifo* f, int on);
 
 /* Channel layout (pointers stay valid until destroy). */

@@ -67,3 +67,14 @@ def test_null_handles_are_rejected(xp):
     assert xp._lib.xp_ring_destroy(None) == xp.XP_OK
     with pytest.raises(xp.XpError):
         xp.xp_set_spin_timeout_ns(10)
+
+
+def test_binding_mirrors_the_header(xp):
+    # the automatic drop threshold and the channel descriptor's last field
+    src = open(HEADER).read()
+    m = re.search(r"#define XP_DISCARD_AUTO_BYTES \(\(size_t\)(\d+) << (\d+)\)", src)
+    assert m and int(m.group(1)) << int(m.group(2)) == xp.XP_DISCARD_AUTO_BYTES
+    body = re.search(r"typedef struct \{((?:(?!typedef struct).)*?)\} xp_channel_desc;", src, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b([a-z_]+);", body)
+    assert fields == [f for f, _ in xp.xp_channel_desc._fields_]

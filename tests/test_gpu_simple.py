@@ -28,11 +28,12 @@ def env():
     return torch, xp
 
 
-def _run_simple(torch, xp, src_np, nchan, nslots, slot, lanes=1, place=0, zero_copy=False, fifo=None):
+def _run_simple(torch, xp, src_np, nchan, nslots, slot, lanes=1, place=0, zero_copy=False, fifo=None, discard=None):
     own = fifo is None
     if own:
         fifo = xp.xp_fifo_create(nchan, nslots, slot, xp.XP_PROTO_SIMPLE, place)
         xp.xp_fifo_set_lanes(fifo, lanes)
+        xp.xp_fifo_set_discard(fifo, discard)   # None: by the FIFO's size
     src = to_dev(torch, src_np)
     dst = torch.zeros_like(src)
     s = torch.cuda.current_stream()
@@ -64,11 +65,13 @@ def test_simple_loopback_workload(env):
     (1, 1, 1, 16, 1), (15, 2, 2, 16, 1), (17, 3, 1, 16, 2), (4095, 3, 2, 64, 1), (65537, 4, 2, 4096, 2),
     (1000003, 16, 8, 16384, 1), (1000003, 5, 3, 65536, 4), (3 << 20, 2, 8, 65536, 8), (777777, 64, 2, 1024, 1),
     (12345, 1, 1, 4096, 3)])
-def test_simple_sweep(env, n, nchan, nslots, slot, lanes):
+@pytest.mark.parametrize("discard", [True, None])
+def test_simple_sweep(env, n, nchan, nslots, slot, lanes, discard):
+    # line drops forced on, and the automatic choice (off for FIFOs this small)
     torch, xp = env
     src = workloads.uniform_bytes(n, seed=n % 1000)
     want, _, _ = oracle.simple_transfer(src, nchan, nslots, slot, seed=1)
-    got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, lanes=lanes)
+    got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, lanes=lanes, discard=discard)
     assert np.array_equal(got, want)
 
 
@@ -211,7 +214,8 @@ def test_simple_receiver_lanes(env, n, nchan, nslots, slot, lanes, rlanes, place
     xp.xp_fifo_set_recv_lanes(fifo, rlanes)
     d = xp.xp_fifo_describe(fifo, 0)
     assert (d.lanes, d.recv_lanes) == (lanes, rlanes)
-    for _ in range(2):
+    for discard in (True, None):
+        xp.xp_fifo_set_discard(fifo, discard)
         got, _ = _run_simple(torch, xp, src, nchan, nslots, slot, fifo=fifo)
         assert np.array_equal(got, want)
     xp.xp_fifo_destroy(fifo)
@@ -319,4 +323,35 @@ def test_slot_contents_only_without_discard(env, discard):
             d = xp.xp_fifo_describe(f, c)
             got = raw_view(torch, d.slots, nslots * slot, "|u1").cpu().numpy()
             assert np.array_equal(got, fo.slots.reshape(-1))
+    xp.xp_fifo_destroy(f)
+
+
+def test_discard_automatic_choice(env):
+    # by default a FIFO drops read slot lines only when its slots take at
+    # least XP_DISCARD_AUTO_BYTES; an explicit setting overrides the choice
+    torch, xp = env
+    T = xp.XP_DISCARD_AUTO_BYTES
+    for (C, N, S), want in (((16, 8, T // 128), 1), ((16, 8, T // 128 - 16), 0), ((1, 8, 65536), 0), ((1, 1, T), 1)):
+        f = xp.xp_fifo_create(C, N, S)
+        assert xp.xp_fifo_describe(f, 0).discard == want
+        for setting, got in ((True, 1), (False, 0), (None, want)):
+            xp.xp_fifo_set_discard(f, setting)
+            assert xp.xp_fifo_describe(f, C - 1).discard == got
+        xp.xp_fifo_destroy(f)
+    # the choice takes effect: a small FIFO left at its default keeps the
+    # oracle's last slot-steps in its slots
+    n, nchan, nslots, slot = 300007, 2, 4, 8192 + 48
+    src_np = workloads.uniform_bytes(n, seed=23)
+    want, fifos, _ = oracle.simple_transfer(src_np, nchan, nslots, slot, seed=4)
+    f = xp.xp_fifo_create(nchan, nslots, slot)
+    xp.xp_fifo_set_lanes(f, 2)
+    src = to_dev(torch, src_np)
+    dst = torch.zeros_like(src)
+    xp.xp_send_recv(f, src, dst, n, torch.cuda.current_stream())
+    assert xp.xp_fifo_status(f, True)[0] == xp.XP_OK
+    assert np.array_equal(from_dev(dst), want)
+    for c, fo in enumerate(fifos):
+        d = xp.xp_fifo_describe(f, c)
+        got = raw_view(torch, d.slots, nslots * slot, "|u1").cpu().numpy()
+        assert np.array_equal(got, fo.slots.reshape(-1))
     xp.xp_fifo_destroy(f)
