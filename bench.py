@@ -706,7 +706,10 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         xs = [torch.from_numpy(x).to("cuda") for x in workloads.ring_inputs(wr["nranks"], nel, "f32", wr["seed_base"])]
         ys = [torch.empty_like(x) for x in xs]
         ring = {}
-        for lanes in (1, 0):   # 0: the library's choice (HBM rings: two lanes, one cooperative grid)
+        # lanes 1: every channel in one launch; 0: the library's choice (channels
+        # in groups of 2 whose live FIFO data stays in L2, 8 lanes, one
+        # cooperative grid of 128 CTAs per group)
+        for lanes in (1, 0):
             r = xp.xp_ring_create(wr["nranks"], wr["nchannels"], wr["nslots"], wr["slot_bytes"])
             try:
                 xp.xp_ring_set_lanes(r, lanes)
@@ -728,6 +731,8 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
                 "ms": ms, "ms_best": min(t), "ms_median": ms, "algbw_gbs": n / (ms * 1e-3) / 1e9,
                 "hbm_gbs": alg / (ms * 1e-3) / 1e9, "frac_of_hbm": alg / (ms * 1e-3) / 1e9 / hbm_peak,
                 "frac_of_ideal_2Pn": ideal / (ms * 1e-3) / 1e9 / hbm_peak,
+                "note": "frac_of_hbm counts the (6P-4)n bytes every slot write and read would move through DRAM; "
+                        "FIFO lines that stay in L2 let it exceed 1, frac_of_ideal_2Pn is the bound",
                 "ranks_agree": bool(all(torch.equal(ys[0], y) for y in ys[1:])), "status": st}
             xp.xp_ring_destroy(r)
         res["ring_f32"] = ring

@@ -142,7 +142,7 @@ struct PingParams {
 
 // Ring FIFOs keep kRingMaxLanes control blocks each: lane g of FIFO f (the
 // bulk-copy ring's independent lanes) uses block f * kRingMaxLanes + g.
-constexpr int kRingMaxLanes = 4;
+constexpr int kRingMaxLanes = 8;
 
 struct RingParams {
   char* ctl;                      // FIFO (c, r) lane g control block at ctl + ((c*nranks + r)*kRingMaxLanes + g)*kCtlBytes
@@ -155,6 +155,7 @@ struct RingParams {
   int nchannels;
   int nslots;
   int lanes;
+  int c_first;                    // bulk-copy ring: first channel of this launch (a launch may run a group of channels)
   int dtype;                      // XP_F32 or XP_I32
   unsigned int slot_bytes;
   DevStatus* status;

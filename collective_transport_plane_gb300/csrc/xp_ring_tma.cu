@@ -10,7 +10,10 @@
 // chunking (and with it the order of every sum) does not depend on G.  The
 // ranks a lane's ring waits on must run at once: the grid is launched
 // cooperatively when all of it fits on the GPU, else as one cluster of P CTAs
-// per (channel, lane), co-resident by construction.  Each CTA moves its
+// per (channel, lane), co-resident by construction.  A launch may cover a
+// group of channels starting at c_first (channels never wait on one
+// another), so the host can run the channels in groups whose live FIFO data
+// stays in L2.  Each CTA moves its
 // stripe through a ring of kRStages stages of two buffers each (A: received
 // slot, or own input for `send`; B: own input for the reducing steps).
 // Threads:
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kRThreads, 1) ring_tma_kernel(const RingParams
   const int G = p.lanes;
   // CTA (c, g, r) = block (c * G + g) * P + r: a cooperative grid, or one
   // cluster of P CTAs per (channel, lane) whose cluster rank is r
-  const int c = (int)(blockIdx.x / P) / G;
+  const int c = p.c_first + (int)(blockIdx.x / P) / G;
   const int g = (int)(blockIdx.x / P) % G;
   const int r = (int)(blockIdx.x % P);
   const unsigned leader = cluster_ctarank();         // every CTA publishes its own lane's counters

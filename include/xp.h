@@ -347,10 +347,14 @@ xp_status xp_ring_create(int nranks, int nchannels, int nslots, size_t slot_byte
                          xp_ring** out);
 xp_status xp_ring_destroy(xp_ring* r);
 
-/* CTAs per rank per channel (0 <= lanes <= 4; default 0).  0 = chosen at
- * each operation: for an HBM ring the largest lane count (at most 4) whose
- * whole grid of nchannels * lanes * nranks CTAs is resident on the GPU at
- * once, at least 1; for a host-placed ring 1.  HBM rings: lane g
+/* CTAs per rank per channel (0 <= lanes <= 8; default 0).  0 = chosen at
+ * each operation: an HBM ring runs its channels in groups, one launch per
+ * group, so that the FIFO data a launch keeps live (nranks * nslots/2 *
+ * slot_bytes per channel) stays within 32 MiB of L2, and gives each group the
+ * largest lane count (at most 8) whose whole grid of group * lanes * nranks
+ * CTAs is resident on the GPU at once, at least 1 (8 ranks x 8 channels of
+ * 8 x 512 KiB: 4 launches of 2 channels at 8 lanes); a host-placed ring
+ * takes 1 lane.  Explicit lanes run every channel in one launch.  HBM rings: lane g
  * moves the g-th 16-byte aligned stripe of every slot-step of every FIFO,
  * with a control block of its own per FIFO (the lanes of a channel are
  * independent rings over disjoint stripes; the result does not depend on

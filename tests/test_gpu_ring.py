@@ -70,7 +70,7 @@ def test_ring_in_place_and_repeated(env):
     xp.xp_ring_destroy(ring)
 
 
-@pytest.mark.parametrize("lanes", [2, 3, 4])
+@pytest.mark.parametrize("lanes", [2, 3, 4, 8])
 @pytest.mark.parametrize("P,n,nchan,nslots,slot", [(8, (1 << 18) + 5, 2, 8, 4096), (3, 100003, 3, 4, 1024),
                                                    (5, 77, 2, 2, 16)])
 def test_ring_lanes(env, lanes, P, n, nchan, nslots, slot):
@@ -100,10 +100,25 @@ def test_ring_lanes_repeated_and_host_placed(env):
         xp.xp_ring_destroy(ring)
 
 
+@pytest.mark.parametrize("P,n,nchan,nslots,slot", [(3, 15000017, 2, 4, 4 << 20), (2, 18000023, 3, 2, 8 << 20)])
+@pytest.mark.parametrize("dtype", ["f32", "i32"])
+def test_ring_channel_groups(env, P, n, nchan, nslots, slot, dtype):
+    # automatic lanes run the channels in groups whose live FIFO data (P x
+    # nslots/2 x slot bytes per channel) fits 32 MiB, one launch per group:
+    # here one channel per launch (24 MiB per channel), and groups of 2 and 1
+    # (16 MiB per channel)
+    torch, xp = env
+    xs = _inputs(P, n, dtype, seed_base=P)
+    want = oracle.ring_order_sum(xs, nchan, nslots, slot)
+    for got in _ring(torch, xp, xs, nchan, nslots, slot, lanes=0):
+        assert np.array_equal(got, want)
+
+
 @pytest.mark.parametrize("dtype,lanes", [("f32", 1), ("i32", 1), ("f32", 0), ("i32", 0)])
 def test_ring_workload(env, dtype, lanes):
-    # 8 ranks x 256 MiB, 8 channels of 8 x 512 KiB per rank-FIFO; lanes 0 lets
-    # the library pick (two lanes, a cooperative grid of 128 CTAs)
+    # 8 ranks x 256 MiB, 8 channels of 8 x 512 KiB per rank-FIFO; lanes 1 runs
+    # every channel in one launch, lanes 0 lets the library pick (groups of 2
+    # channels at 8 lanes, four cooperative grids of 128 CTAs)
     torch, xp = env
     w = workloads.RING
     xs = _inputs(w["nranks"], w["nelems"], dtype, w["seed_base"])
