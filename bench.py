@@ -291,6 +291,7 @@ def main():
     if args.mode == "ll128":
         fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
         xp.xp_fifo_set_lanes(fifo, min(args.lanes, 8))
+        xp.xp_fifo_set_recv_lanes(fifo, min(args.rlanes, 8))
     else:
         fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"])
         xp.xp_fifo_set_lanes(fifo, args.lanes)
@@ -355,7 +356,7 @@ def main():
         "config": {"workload": "SIMPLE multi-channel: 1 GiB bf16 N(0,1) seed 2, 16 channels x 8 slots x 512 KiB, FIFO in HBM",
                    "nchannels": w["nchannels"], "nslots": w["nslots"], "slot_bytes": w["slot_bytes"],
                    "sender_ctas_per_channel": min(args.lanes, 8) if args.mode == "ll128" else args.lanes,
-                   "receiver_ctas_per_channel": min(args.lanes, 8) if args.mode == "ll128" else args.rlanes,
+                   "receiver_ctas_per_channel": min(args.rlanes, 8) if args.mode == "ll128" else args.rlanes,
                    "payload_bytes": nbytes, "parallelism": f"replicas{world}",
                    "l2": "inputs (1 GiB) larger than L2; the 64 MiB FIFO itself is L2-resident by design"},
         "gpu_launches": args.steps,
@@ -609,9 +610,12 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
         dst = torch.empty_like(src)
         n = src.numel() * 2
         multi = {}
-        for lanes in (1, 2, 4):
+        # sender:receiver CTAs per channel; 4:5 fills 144 of the 152 SMs (the
+        # receivers are the slower side)
+        for lanes, rlanes in ((1, 1), (2, 2), (4, 4), (4, 5)):
             f = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
             xp.xp_fifo_set_lanes(f, lanes)
+            xp.xp_fifo_set_recv_lanes(f, rlanes)
             dst.zero_()
             with torch.cuda.stream(s):
                 for _ in range(3):
@@ -619,7 +623,8 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
                 t = time_events(torch, s, lambda: xp.xp_send_recv(f, src, dst, n, s), 10)
             st2, _ = xp.xp_fifo_status(f, True)
             ms = statistics.median(t)
-            multi[f"lanes{lanes}"] = {"gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "ms_best": min(t), "ms_median": ms,
+            multi[f"lanes{lanes}" if lanes == rlanes else f"lanes{lanes}_recv{rlanes}"] = {
+                                      "gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "ms_best": min(t), "ms_median": ms,
                                       "frac_of_hbm": (2 + 2 * 128 / 120) * n / (ms * 1e-3) / 1e9 / hbm_peak,
                                       "exact": bool(st2 == xp.XP_OK and torch.equal(dst, src))}
             xp.xp_fifo_destroy(f)

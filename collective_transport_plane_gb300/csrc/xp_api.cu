@@ -515,9 +515,10 @@ xp_status xp_fifo_enable_ce(xp_fifo* f) {
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
   if (f->proto == XP_PROTO_LL128) {
-    // independent lanes: a cluster of a sender and a receiver CTA each, a
-    // head of its own each (lane 0: the channel's head word, lanes 1 .. 7:
-    // lines of the channel's arrival block)
+    // sender and receiver lanes (the receiver side may then be changed with
+    // xp_fifo_set_recv_lanes); each receiver lane keeps a head of its own
+    // (lane 0: the channel's head word, lanes 1 .. 7: lines of the channel's
+    // arrival block)
     if (lanes < 1 || lanes > 8) return fail(XP_ERR_INVALID, "LL128 lanes %d not in [1, 8]", lanes);
     f->lanes = f->rlanes = lanes;
     return XP_OK;
@@ -531,7 +532,12 @@ xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes) {
 
 xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes) {
   if (!f) return fail(XP_ERR_INVALID, "fifo is NULL");
-  if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE FIFOs only");
+  if (f->proto == XP_PROTO_LL128) {
+    if (rlanes < 1 || rlanes > 8) return fail(XP_ERR_INVALID, "LL128 receiver lanes %d not in [1, 8]", rlanes);
+    f->rlanes = rlanes;
+    return XP_OK;
+  }
+  if (f->proto != XP_PROTO_SIMPLE) return fail(XP_ERR_INVALID, "lanes apply to SIMPLE and LL128 FIFOs only");
   if (rlanes < 1 || rlanes > xp::kMaxLanes) return fail(XP_ERR_INVALID, "receiver lanes %d not in [1, 32]", rlanes);
   f->rlanes = rlanes;
   return XP_OK;
@@ -618,10 +624,11 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
   int csize, block, smem = 0;
   if (f->proto != XP_PROTO_SIMPLE) {
     kernel = f->proto == XP_PROTO_LL ? xp::ll_kernel_ptr() : xp::ll128_kernel_ptr();
-    // one cluster of a sender and a receiver CTA per channel (LL) or per
-    // lane of a channel (LL128)
+    // LL: one cluster of a sender and a receiver CTA per channel; LL128: the
+    // channel's sender lanes, then its receiver lanes
     p.lanes = f->proto == XP_PROTO_LL ? 1 : f->lanes;
-    csize = 2;
+    p.rlanes = f->proto == XP_PROTO_LL ? 1 : f->rlanes;
+    csize = p.lanes + p.rlanes;
     block = f->proto == XP_PROTO_LL ? xp::kLLThreads : xp::ll128_threads();
     if (f->proto == XP_PROTO_LL128) smem = xp::ll128_smem();
   } else {
@@ -640,18 +647,19 @@ static xp_status p2p_op(xp_fifo* f, const void* src, void* dst, size_t bytes, xp
     }
   }
   p.csize = csize;
-  // The bulk-copy kernel needs the sender and receiver CTAs of a channel
-  // resident together: a cooperative grid when all of it fits at once (no
-  // cluster placement limits), else one cluster per channel.  The other
-  // kernels always use clusters.
+  // The bulk-copy and LL128 kernels need the sender and receiver CTAs of a
+  // channel resident together: a cooperative grid when all of it fits at
+  // once (no cluster placement limits), else one cluster per channel.  The
+  // other kernels always use clusters.
   int launch_csize = csize;
-  if (kernel == xp::p2p_tma_kernel_ptr(mode) && f->C * csize <= resident_ctas(kernel, block, smem))
+  if ((kernel == xp::p2p_tma_kernel_ptr(mode) || kernel == xp::ll128_kernel_ptr()) &&
+      f->C * csize <= resident_ctas(kernel, block, smem))
     launch_csize = 0;
   if (launch_csize > xp::kMaxCluster)
     return fail(XP_ERR_INVALID, "%d channels x %d CTAs neither fit on the GPU at once nor form clusters of at most 16",
                 f->C, csize);
   p.op = ++f->cm.ops;
-  const int grid = f->proto == XP_PROTO_SIMPLE ? f->C * csize : f->C * p.lanes * 2;
+  const int grid = f->C * csize;
   if ((s = launch(kernel, grid, block, launch_csize, &p, st, smem)) != XP_OK) return s;
   if (mode == kOpProxy) xp::pump_kick(f->pump);
   return record_done(f->cm, st);

@@ -10,21 +10,25 @@
 // be visible first.  PTX promises single-copy atomicity per element only,
 // not for a 128-byte line ("RDMA and GPUDirect" §8 makes the same point for
 // a NIC's writes: seeing the flag does not mean the data has landed), so
-// the order is made explicit and paid for once per batch of lines instead
+// the order is made explicit and paid for once per chunk of lines instead
 // of once per line:
-//   sender   — store the payload of kBatch lines per thread, __syncwarp,
-//              fence (release), store the batch's flags;
+//   sender   — the copy warps store a chunk's payload (kBatch lines per
+//              thread) and arrive on the chunk's barrier (release); a
+//              flagger warp waits for it, fences once and stores the
+//              chunk's flags, so the copy warps never wait on a fence;
 //   receiver — poll the batch's flags (one of them with acquire), __syncwarp,
 //              load the batch's payload.
-// There is no tail; head returns slot credit.  A channel runs on G
-// independent lanes, each a cluster of two CTAs (sender, receiver): lane g
-// owns the same fixed stripe of ceil(L / G) lines of every slot and keeps a
-// head of its own, so the lanes of a channel never wait for one another.
-// The receiver's copy warps arrive on a per-slot mbarrier and its publisher
-// warp stores the lane's head.  The last lane of a channel to finish an
-// operation moves the channel's step base on and sets every lane's head to
-// it, so the next operation may cut the slots into a different number of
-// stripes.
+// There is no tail; head returns slot credit.  A channel runs on G sender
+// and GR receiver CTAs ("lanes"), consecutive in the grid and resident
+// together (a cooperative grid, else one cluster per channel): sender lane g
+// owns the fixed stripe of ceil(L / G) lines of every slot, receiver lane r
+// that of ceil(L / GR) lines, and each receiver lane keeps a head of its own;
+// a sender lane refills a slot's stripe once every receiver lane whose
+// stripe meets it has returned the credit.  The receiver's copy warps
+// arrive on a per-slot mbarrier and its publisher warp stores the lane's
+// head.  The last receiver lane of a channel to finish an operation moves
+// the channel's step base on and sets every lane's head to it, so the next
+// operation may cut the slots into different stripes.
 #include <cuda_runtime.h>
 
 #include "xp_device.cuh"
@@ -33,11 +37,11 @@ namespace xp {
 
 namespace {
 
-constexpr int kL128Warps = 16;     // copy warps per CTA (one more warp: producer or publisher)
-constexpr int kL128Threads = 32 * (kL128Warps + 1);
+constexpr int kL128Warps = 16;     // copy warps per CTA (two more: producer and flagger, or publisher)
+constexpr int kL128Threads = 32 * (kL128Warps + 2);
 constexpr u64 kLineBytes = 128;
 constexpr u64 kDataWords = 15;
-constexpr int kBatch = 8;          // lines per thread between two fences
+constexpr int kBatch = 8;          // lines per thread per chunk
 constexpr u64 kChunkLines = 32ull * kL128Warps / 8 * kBatch;   // lines the copy warps write per stage
 // a stage holds a chunk's payload from the 16-byte boundary at or below its
 // first byte: at most 8 bytes of lead plus 120 bytes per line
@@ -101,31 +105,40 @@ __device__ __forceinline__ u64 ld_word(const void* p) {
 __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams p) {
   extern __shared__ __align__(128) unsigned char stage_mem[];
   __shared__ __align__(8) u64 bars[kMaxSlots];
-  __shared__ __align__(8) u64 full[kStages], empty[kStages];
+  __shared__ __align__(8) u64 full[kStages], empty[kStages], pdone[kStages];
   __shared__ u64 s_base;
   __shared__ int s_stop;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const unsigned crank = cluster_ctarank();
+  // Channel ch runs G sender and GR receiver CTAs, consecutive in the grid
+  // (a cooperative grid, or one cluster per channel).
   const unsigned G = (unsigned)p.lanes;
-  const unsigned pair = blockIdx.x / 2;
-  const int ch = (int)(pair / G);
-  const unsigned g = pair % G;                 // lane
-  const bool sender = crank == 0;
+  const unsigned GR = (unsigned)p.rlanes;
+  const int ch = (int)(blockIdx.x / (G + GR));
+  const unsigned crank = blockIdx.x % (G + GR);
+  const bool sender = crank < G;
+  const unsigned g = sender ? crank : crank - G;   // lane within the side
   const u64 N = (u64)p.nslots;
   const u64 L = p.slot_bytes / kLineBytes;     // lines per slot
   const u64 W = L * kDataWords;                // payload words per slot-step
-  const u64 Lg = (L + G - 1) / G;              // stripe of lines per lane
-  const u64 l0 = g * Lg;
+  const u64 LgS = (L + G - 1) / G;             // stripe of lines per sender lane
+  const u64 LgR = (L + GR - 1) / GR;           // and per receiver lane
+  const u64 Lg = sender ? LgS : LgR;
+  const u64 l0 = g * Lg < L ? g * Lg : L;
   const u64 l1 = l0 + Lg < L ? l0 + Lg : L;
 
   char* ctl = p.ctl + (u64)ch * kCtlBytes;
-  // lane 0's head is the channel's head word; lanes 1 .. 7 keep theirs on
-  // lines 1 .. 7 of the channel's block of the arrival region, whose line 0
-  // counts the lanes that have finished the operation
+  // receiver lane 0's head is the channel's head word; lanes 1 .. 7 keep
+  // theirs on lines 1 .. 7 of the channel's block of the arrival region, whose
+  // line 0 counts the receiver lanes that have finished the operation
   u64* arr = p.arr + (u64)ch * (kArrBytes / 8);
-  u64* head = g == 0 ? reinterpret_cast<u64*>(ctl + kHeadOff) : arr + 16 * g;
+  auto head_of = [&](unsigned rl) { return rl == 0 ? reinterpret_cast<u64*>(ctl + kHeadOff) : arr + 16 * rl; };
+  u64* head = head_of(g);   // the receiver's own
+  // a sender lane refills a slot's lines [l0, l1) once every receiver lane
+  // whose stripe meets them has returned the credit
+  const unsigned rlo = sender && l1 > l0 ? (unsigned)(l0 / LgR) : 0;
+  const unsigned rhi = sender && l1 > l0 ? (unsigned)((l1 - 1) / LgR) : 0;
   u64* basew = reinterpret_cast<u64*>(ctl + kBaseOff);
   char* slots = p.slots + (u64)ch * p.ch_stride;
 
@@ -146,14 +159,16 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
     if (sender) {
       for (int k = 0; k < kStages; ++k) {
         mbar_init(smem_addr(&full[k]), 1);
-        mbar_init(smem_addr(&empty[k]), kL128Warps);
+        mbar_init(smem_addr(&empty[k]), kL128Warps + 1);   // the copy warps and the flagger
+        mbar_init(smem_addr(&pdone[k]), kL128Warps);       // the chunk's payload is stored
       }
       mbar_init_fence();
     }
   }
-  // Each CTA's barriers are its own (no shared memory is used across the
-  // pair), so a block barrier is enough here and none is needed at the end;
-  // the cluster launch still schedules the pair together.
+  // Each CTA's barriers are its own (no shared memory is used across CTAs),
+  // so a block barrier is enough here and none is needed at the end; the
+  // launch (cooperative, or a cluster per channel) keeps the channel's CTAs
+  // resident together.
   __syncthreads();
   const u64 base = s_base;
   const bool run = nsteps > 0 && s_stop == 0;
@@ -181,12 +196,16 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
       // The producer thread (below) stages each chunk of the lane's payload
       // in shared memory with a bulk copy; the copy warps turn it into lines.
       const uint32_t sm0 = smem_addr(stage_mem);
-      u64 hcache = 0;
+      u64 hcache[kMaxLL128Lanes] = {};
       u64 j = 0;           // chunks consumed
       int failed = 0;
       for (u64 s = 0; s < nsteps && !failed; ++s) {
         const u64 step = base + s;
-        if (step + 1 > N && !warp_wait_geq(head, step + 1 - N, hcache, w, XP_WAIT_HEAD)) break;
+        if (step + 1 > N && l1 > l0) {
+          for (unsigned rl = rlo; rl <= rhi && !failed; ++rl)
+            if (!warp_wait_geq(head_of(rl), step + 1 - N, hcache[rl], w, XP_WAIT_HEAD)) failed = 1;
+          if (failed) break;
+        }
         const u64 left = nwords - s * W;
         const u64 nla = left >= W ? L : (left + kDataWords - 1) / kDataWords;
         const u64 nl = nla < l1 ? nla : l1;         // end of this lane's lines in the step
@@ -223,12 +242,9 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
               }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_local_relaxed(smem_addr(&empty[k]));
-            fence_gpu();
-            if (flag_lane) {
-#pragma unroll
-              for (int q = 0; q < kBatch; ++q)
-                if (i0 + q * P < c1) st_flag(line + 8 + q * kRowLines, flag);
+            if (lane == 0) {
+              mbar_arrive_local_relaxed(smem_addr(&empty[k]));
+              mbar_arrive_local(smem_addr(&pdone[k]));
             }
             continue;
           }
@@ -258,20 +274,14 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
           }
           // the stage's values are in registers (the stores above used them)
           __syncwarp();
-          if (lane == 0) mbar_arrive_local_relaxed(smem_addr(&empty[k]));
-          // every payload store of the warp's lines before any of their flags
-          fence_gpu();
-          if (flag_lane) {
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-              const u64 i = i0 + q * P;
-              if (i < c1) st_flag(slot + i * kLineBytes + 8 * kDataWords, flag);
-            }
+          if (lane == 0) {
+            mbar_arrive_local_relaxed(smem_addr(&empty[k]));
+            mbar_arrive_local(smem_addr(&pdone[k]));
           }
         }
       }
     } else {
-      const uint32_t bar0 = map_to_rank(smem_addr(&bars[0]), 1);
+      const uint32_t bar0 = map_to_rank(smem_addr(&bars[0]), cluster_ctarank());
       int failed = 0;
       u64 hcache = 0;
       for (u64 r = 0; r < nsteps && !failed; ++r) {
@@ -405,6 +415,31 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
         if (nb) bulk_load(sm0 + k * kStageBytes, p.src + a0, nb, smem_addr(&full[k]), pol);
       }
     }
+  } else if (run && warp == kL128Warps + 1 && sender) {
+    // flagger: once every copy warp has stored a chunk's payload, one fence
+    // per lane orders it before the chunk's flags, which the warp stores
+    u64 j = 0;
+    bool ok = true;
+    for (u64 s = 0; s < nsteps && ok; ++s) {
+      const u64 step = base + s;
+      const u64 left = nwords - s * W;
+      const u64 nla = left >= W ? L : (left + kDataWords - 1) / kDataWords;
+      const u64 nl = nla < l1 ? nla : l1;
+      const u64 flag = step + 1;
+      char* slot = slots + (step % N) * p.slot_bytes;
+      for (u64 c0 = l0; c0 < nl; c0 += kChunkLines, ++j) {
+        const int k = (int)(j % kStages);
+        if (!mbar_wait_cta(smem_addr(&pdone[k]), (uint32_t)((j / kStages) & 1), w)) {
+          ok = false;
+          break;
+        }
+        fence_gpu();
+        const u64 c1 = c0 + kChunkLines < nl ? c0 + kChunkLines : nl;
+        for (u64 i = c0 + lane; i < c1; i += 32) st_flag(slot + i * kLineBytes + 8 * kDataWords, flag);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local_relaxed(smem_addr(&empty[k]));
+      }
+    }
   } else if (run && warp == kL128Warps && lane == 0 && !sender) {
     u64 r = 0;
     for (; r < nsteps; ++r) {
@@ -416,7 +451,7 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
       // every lane has read the step base at its start; the last one to
       // finish moves it on and leaves every lane's head there
       const u64 done = atom_add_acq_rel(arr, 1);
-      if (done + 1 == G) {
+      if (done + 1 == GR) {
         const u64 nb = base + nsteps;
         st_relaxed(reinterpret_cast<u64*>(ctl + kHeadOff), nb);
         for (int h = 1; h < kMaxLL128Lanes; ++h) st_relaxed(arr + 16 * h, nb);

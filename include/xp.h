@@ -166,20 +166,26 @@ xp_status xp_fifo_destroy(xp_fifo* f);
  * else as one thread-block cluster per channel, which needs sender + receiver
  * CTAs <= 16; an operation that fits neither way is refused (XP_ERR_INVALID).
  * Host-placed FIFOs always use clusters.  LL128 FIFOs: 1 <= lanes <= 8
- * independent lanes per channel, each a cluster of a sender and a receiver
- * CTA with a head of its own, lane g moving the same fixed stripe of
- * ceil(L / lanes) of each slot's L lines; at the end of an operation every
- * lane's head equals the channel's step base, so the count may change from
+ * sender and as many receiver CTAs per channel (xp_fifo_set_recv_lanes may
+ * then change the receiver side), sender lane g moving the fixed stripe of
+ * ceil(L / lanes) of each slot's L lines and receiver lane r that of
+ * ceil(L / rlanes) lines with a head of its own; a sender lane refills its
+ * stripe of a slot once every receiver lane whose stripe meets it has
+ * returned the credit.  The channel's CTAs run as one cooperative grid when
+ * nchannels x (lanes + rlanes) are resident at once, else as one cluster
+ * per channel (lanes + rlanes <= 16).  At the end of an operation every
+ * lane's head equals the channel's step base, so the counts may change from
  * one operation to the next.  LL FIFOs: refused.  Takes effect at the next
  * operation. */
 xp_status xp_fifo_set_lanes(xp_fifo* f, int lanes);
 
 /* Receiver CTAs per channel of xp_send_recv, independently of the sender's
- * (1 <= rlanes <= 32; the launch rules of xp_fifo_set_lanes apply): the
- * slot-step is published whole, so the receiver may cut it into a different
- * number of stripes (also for copy-mode posted and proxy transfers).  Zero
- * copy and direct posted transfers always use one receiver CTA.  SIMPLE FIFOs
- * only. */
+ * (SIMPLE: 1 <= rlanes <= 32; LL128: 1 <= rlanes <= 8; the launch rules of
+ * xp_fifo_set_lanes apply): the slot-step is published whole (SIMPLE) or
+ * line by line (LL128), so the receiver may cut it into a different number
+ * of stripes (also for copy-mode posted and proxy transfers).  Zero copy and
+ * direct posted transfers always use one receiver CTA.  LL FIFOs: refused.
+ * Takes effect at the next operation (xp_fifo_set_lanes resets it). */
 xp_status xp_fifo_set_recv_lanes(xp_fifo* f, int rlanes);
 
 /* Whether receivers that read FIFO slots in HBM drop each 128-byte line of

@@ -99,6 +99,27 @@ def test_ll128_sweep(env, n, nchan, nslots, slot, lanes):
     xp.xp_fifo_destroy(fifo)
 
 
+@pytest.mark.parametrize("lanes,rlanes", [(1, 2), (2, 1), (3, 5), (4, 5), (5, 3), (1, 8), (8, 3)])
+@pytest.mark.parametrize("n,nchan,nslots,slot", [SWEEP[2], SWEEP[3], SWEEP[5], SWEEP[7], SWEEP[8]])
+def test_ll128_receiver_lanes(env, n, nchan, nslots, slot, lanes, rlanes):
+    # sender and receiver sides cut each slot into different stripes: a
+    # sender lane waits for the credit of every receiver lane its stripe
+    # meets; twice through the same FIFO
+    torch, xp = env
+    src = workloads.uniform_bytes(n, seed=n % 89)
+    fifo = xp.xp_fifo_create(nchan, nslots, slot, xp.XP_PROTO_LL128)
+    xp.xp_fifo_set_lanes(fifo, lanes)
+    xp.xp_fifo_set_recv_lanes(fifo, rlanes)
+    d = xp.xp_fifo_describe(fifo, 0)
+    assert (d.lanes, d.recv_lanes) == (lanes, rlanes)
+    fifos = None
+    for k in range(2):
+        want, fifos, _ = oracle.ll128_transfer(src, nchan, nslots, slot, seed=k, fifos=fifos)
+        assert np.array_equal(_ll128(torch, xp, fifo, src), want.view(np.uint8))
+        _check_slots(torch, xp, fifo, fifos, nslots, slot)
+    xp.xp_fifo_destroy(fifo)
+
+
 @pytest.mark.parametrize("lanes", [1, 2])
 def test_ll128_host_placed(env, lanes):
     torch, xp = env
@@ -117,25 +138,27 @@ def test_ll128_lanes_change_between_operations(env):
     torch, xp = env
     fifo = xp.xp_fifo_create(3, 2, 1024, xp.XP_PROTO_LL128)
     fifos = None
-    for i, lanes in enumerate((1, 4, 2, 8, 3, 1)):
+    for i, (lanes, rlanes) in enumerate(((1, 1), (4, 4), (2, 5), (8, 8), (3, 3), (1, 1), (6, 2), (2, 7))):
         src = workloads.uniform_bytes(20000 + 968 * i, seed=30 + i)
         xp.xp_fifo_set_lanes(fifo, lanes)
+        xp.xp_fifo_set_recv_lanes(fifo, rlanes)
         want, fifos, _ = oracle.ll128_transfer(src, 3, 2, 1024, seed=i, fifos=fifos)
         assert np.array_equal(_ll128(torch, xp, fifo, src), want.view(np.uint8)), lanes
         _check_slots(torch, xp, fifo, fifos, 2, 1024)
     xp.xp_fifo_destroy(fifo)
 
 
-@pytest.mark.parametrize("lanes", [1, 4])
-def test_ll128_workload(env, lanes):
+@pytest.mark.parametrize("lanes,rlanes", [(1, 1), (4, 4), (4, 5)])
+def test_ll128_workload(env, lanes, rlanes):
     # 1 GiB of bf16 normals through 16 channels of 8 x 512 KiB LL128 slots:
     # identity, and the slots of the first and last channel by the format's
-    # definition
+    # definition (4 + 5 lanes is the configuration bench.py times)
     torch, xp = env
     w = workloads.SIMPLE_MULTI
     src_np = workloads.normal_bf16_bits(w["nelems"], w["seed"]).view(np.uint8)
     fifo = xp.xp_fifo_create(w["nchannels"], w["nslots"], w["slot_bytes"], xp.XP_PROTO_LL128)
     xp.xp_fifo_set_lanes(fifo, lanes)
+    xp.xp_fifo_set_recv_lanes(fifo, rlanes)
     assert np.array_equal(_ll128(torch, xp, fifo, src_np), src_np)
     words = src_np.view(np.uint64)
     ranges = oracle.channel_byte_ranges(src_np.nbytes, w["nchannels"])
@@ -162,7 +185,8 @@ def test_ll128_argument_errors(env):
                  lambda: xp.xp_send_recv_posted(f, a, b, 64, False, torch.cuda.current_stream()),
                  lambda: xp.xp_fifo_enable_ce(f),
                  lambda: xp.xp_fifo_set_lanes(f, 9),
-                 lambda: xp.xp_fifo_set_recv_lanes(f, 2)):
+                 lambda: xp.xp_fifo_set_recv_lanes(f, 9),
+                 lambda: xp.xp_fifo_set_recv_lanes(f, 0)):
         with pytest.raises(xp.XpError) as e:
             call()
         assert e.value.status == xp.XP_ERR_INVALID
