@@ -303,11 +303,12 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
           const char* line = slot + i0 * kLineBytes + 16 * pos;
           // Every flag of the batch is polled with relaxed loads, all in
           // flight together, except the last line's (the anchor), which is
-          // loaded with acquire.  The sender warp that wrote these lines
-          // stored all of their payload before one fence and their flags
-          // after it, so the acquire that sees the anchor's flag makes the
-          // payload of every line of the batch visible to the loads below
-          // (the warp barrier passes that on to the other threads).
+          // loaded with acquire.  The sender's copy warps stored the payload
+          // of the whole chunk holding these lines before the flagger's
+          // fence, and the flagger stored their flags after it, so the
+          // acquire that sees the anchor's flag makes the payload of every
+          // line of the batch visible to the loads below (the warp barrier
+          // passes that on to the other threads).
           int ok = 1;
           if (flag_lane) {
             unsigned todo = 0;
