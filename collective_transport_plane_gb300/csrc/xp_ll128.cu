@@ -295,6 +295,9 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
         const u64 flag = step + 1;
         const char* slot = slots + (step % N) * p.slot_bytes;
         u64* sdst = dst + r * W;
+        // first sender-lane boundary above this thread's lines (a batch that
+        // crosses one holds lines of two senders, ordered by two fences)
+        u64 nb = ((u64)((uint32_t)(wline + sub) / (uint32_t)LgS) + 1) * LgS;
         for (u64 w0 = wline; w0 < nl && !failed; w0 += P * kBatch) {
           const u64 i0 = w0 + sub;
           // every line of the step up to nl carries payload in every word:
@@ -303,12 +306,18 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
           const char* line = slot + i0 * kLineBytes + 16 * pos;
           // Every flag of the batch is polled with relaxed loads, all in
           // flight together, except the last line's (the anchor), which is
-          // loaded with acquire.  The sender's copy warps stored the payload
-          // of the whole chunk holding these lines before the flagger's
-          // fence, and the flagger stored their flags after it, so the
-          // acquire that sees the anchor's flag makes the payload of every
-          // line of the batch visible to the loads below (the warp barrier
-          // passes that on to the other threads).
+          // loaded with acquire, and, when the batch's lines cross from one
+          // sender lane's stripe into the next, also the last line before
+          // the boundary.  A sender's copy warps store a chunk's payload
+          // before its flagger's fence for the chunk, and the flagger stores
+          // the chunk's flags after that fence; the flagger takes its chunks
+          // in order, so that fence also follows the payload of the lane's
+          // earlier chunks.  An acquire that sees a flag therefore makes the
+          // payload of every line of the batch from that sender lane, up to
+          // that line, visible to the loads below (the warp barrier passes
+          // that on to the other threads).  A batch whose lines come from
+          // three or more sender lanes (stripes shorter than the batch)
+          // loads every flag with acquire.
           int ok = 1;
           if (flag_lane) {
             unsigned todo = 0;
@@ -316,21 +325,44 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
             for (int q = 0; q < kBatch; ++q)
               if (i0 + q * P < nl) todo |= 1u << q;
             const unsigned anchor = todo ? 1u << (31 - __clz(todo)) : 0u;
+            while (nb <= i0) nb += LgS;
+            unsigned anchor2 = 0;
+            bool every = false;   // three or more senders: every flag with acquire
+            if (anchor) {
+              const u64 itop = i0 + (31 - __clz(anchor)) * P;
+              if (itop >= nb + LgS) every = true;
+              else if (itop >= nb) anchor2 = 1u << (unsigned)((nb - 1 - i0) / P);
+            }
             WaitClock clk;
             unsigned it = 0;
             while (todo) {
               u64 seen = 0;
+              if (every) {
 #pragma unroll
-              for (int q = 0; q < kBatch; ++q)
-                if ((todo & ~anchor) & (1u << q)) {
-                  const u64 f = ld_flag(line + 8 + q * kRowLines);
-                  if (f == flag) todo &= ~(1u << q);
+                for (int q = 0; q < kBatch; ++q)
+                  if (todo & (1u << q)) {
+                    const u64 f = ld_flag_acquire(line + 8 + q * kRowLines);
+                    if (f == flag) todo &= ~(1u << q);
+                    else seen = f;
+                  }
+              } else {
+#pragma unroll
+                for (int q = 0; q < kBatch; ++q)
+                  if ((todo & ~(anchor | anchor2)) & (1u << q)) {
+                    const u64 f = ld_flag(line + 8 + q * kRowLines);
+                    if (f == flag) todo &= ~(1u << q);
+                    else seen = f;
+                  }
+                if (todo & anchor2) {
+                  const u64 f = ld_flag_acquire(line + 8 + (31 - __clz(anchor2)) * kRowLines);
+                  if (f == flag) todo &= ~anchor2;
                   else seen = f;
                 }
-              if (todo & anchor) {
-                const u64 f = ld_flag_acquire(line + 8 + (31 - __clz(anchor)) * kRowLines);
-                if (f == flag) todo &= ~anchor;
-                else seen = f;
+                if (todo & anchor) {
+                  const u64 f = ld_flag_acquire(line + 8 + (31 - __clz(anchor)) * kRowLines);
+                  if (f == flag) todo &= ~anchor;
+                  else seen = f;
+                }
               }
               if (todo && (++it & 7u) == 0 && !clk.tick(w, XP_WAIT_LL_FLAG, seen, flag)) {
                 ok = 0;
