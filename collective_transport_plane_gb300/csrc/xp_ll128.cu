@@ -209,7 +209,6 @@ __global__ void __launch_bounds__(kL128Threads, 1) ll128_kernel(const P2pParams 
         const u64 left = nwords - s * W;
         const u64 nla = left >= W ? L : (left + kDataWords - 1) / kDataWords;
         const u64 nl = nla < l1 ? nla : l1;         // end of this lane's lines in the step
-        const u64 flag = step + 1;
         char* slot = slots + (step % N) * p.slot_bytes;
         const u64 sbyte = lo + 8 * s * W;           // src offset of the step's first payload word
         for (u64 c0 = l0; c0 < nl; c0 += kChunkLines, ++j) {
