@@ -16,8 +16,9 @@
 //              thread) and arrive on the chunk's barrier (release); a
 //              flagger warp waits for it, fences once and stores the
 //              chunk's flags, so the copy warps never wait on a fence;
-//   receiver — poll the batch's flags (one of them with acquire), __syncwarp,
-//              load the batch's payload.
+//   receiver — poll the batch's flags (with acquire one per sender lane the
+//              batch's lines come from, the rest relaxed), __syncwarp, load
+//              the batch's payload.
 // There is no tail; head returns slot credit.  A channel runs on G sender
 // and GR receiver CTAs ("lanes"), consecutive in the grid and resident
 // together (a cooperative grid, else one cluster per channel): sender lane g
