@@ -26,7 +26,8 @@ arithmetic rounded to fp32, against int64 sums for int32, against the
 fp64 sum within the standard error bound, and the pages' printed sizes and
 ring-neighbour example (tests/golden/).
 """
-from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, Deadlock, LL128Fifo, LL128Receiver, LL128Sender, LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender,
+from .fifo import (CEFifo, CEProxy, CEReceiver, CESender, Deadlock, LL128Fifo, LL128LaneFifo, LL128LaneReceiver,
+                   LL128LaneSender, LL128Receiver, LL128Sender, LLFifo, LLReceiver, LLSender, PostedChannel, PostedReceiver, PostedSender,
                    ProtocolViolation, SimpleFifo, SimpleReceiver, SimpleSender, System, ZeroCopyChannel,
                    ZeroCopyReceiver, ZeroCopySender, explore, ll128_flag, ll_flag, run)
 from .partition import (channel_byte_ranges, ring_channel_ranges, ring_chunk_elems, ring_next,
@@ -44,4 +45,5 @@ __all__ = [
     "PostedChannel", "PostedSender", "PostedReceiver", "posted_transfer",
     "CEFifo", "CESender", "CEProxy", "CEReceiver", "ce_transfer",
     "LL128Fifo", "LL128Sender", "LL128Receiver", "ll128_flag", "ll128_transfer",
+    "LL128LaneFifo", "LL128LaneSender", "LL128LaneReceiver",
 ]

@@ -678,6 +678,171 @@ class LL128Receiver(Actor):
         return (self.step, self.line, self.pub, self.early, snap)
 
 
+class LL128LaneFifo(LL128Fifo):
+    """An LL128 channel whose receiver side is cut into `rlanes` lanes (our
+    design; the pages have one receiver per channel): receiver lane r owns
+    lines [r*LgR, (r+1)*LgR) of every slot, LgR = ceil(L / rlanes), and keeps
+    a head of its own."""
+
+    def __init__(self, nslots: int, slot_bytes: int, rlanes: int, step0: int = 0):
+        super().__init__(nslots, slot_bytes, step0)
+        self.GR = rlanes
+        self.LgR = ceil_div(self.L, rlanes)
+        self.heads = [step0] * rlanes
+
+    def rlane(self, line: int) -> int:
+        return line // self.LgR
+
+    def check(self):
+        pass   # the per-line overwrite check in the senders is the invariant
+
+    def state(self):
+        return (tuple(self.heads), self.lines.tobytes(), self.owner.tobytes())
+
+
+class LL128LaneSender(Actor):
+    """Sender lane g of `lanes`: writes lines [g*LgS, (g+1)*LgS) of every
+    slot-step of words[lo:hi], LgS = ceil(L / lanes), as LL128Sender writes
+    whole steps (payload words visible one piece at a time, the batch's flags
+    only after all its payload).  It fills its lines of step s only once every
+    receiver lane whose lines meet its own has head > s - N; a payload piece
+    that becomes visible while the receiver lane owning its line has not
+    returned that credit is a protocol violation.  `fault`: "one_lane_credit"
+    (wait only for the first receiver lane its lines meet)."""
+
+    def __init__(self, fifo: LL128LaneFifo, words: np.ndarray, lo: int, hi: int, lanes: int, lane: int,
+                 batch: int = 1, piece_words: int = LL128_DATA_WORDS, fault: str | None = None):
+        self.f, self.words, self.lo, self.hi = fifo, words, lo, hi
+        self.nwords = hi - lo
+        self.base = fifo.heads[0]
+        self.nsteps = ceil_div(self.nwords, fifo.L * LL128_DATA_WORDS)
+        lg = ceil_div(fifo.L, lanes)
+        self.l0 = min(lane * lg, fifo.L)
+        self.l1 = min(self.l0 + lg, fifo.L)
+        self.rlanes = sorted({fifo.rlane(i) for i in range(self.l0, self.l1)})
+        if fault == "one_lane_credit":
+            self.rlanes = self.rlanes[:1]
+        self.step = self.base
+        self.line = self.l0
+        self.granted = False
+        self.batch, self.pw = batch, piece_words
+        self.in_batch: list[tuple[int, int, int]] = []
+        self.pending: list[_Piece] = []
+        self.name = f"ll128-send-lane{lane}[{lo}:{hi}]"
+        self._skip_empty()
+
+    def _end(self, step):
+        return min(self.l1, _ll128_lines(self.nwords, self.f.L, step - self.base))
+
+    def _skip_empty(self):
+        while self.step < self.base + self.nsteps and self.l0 >= self._end(self.step) and not self.in_batch:
+            self.step += 1
+
+    def done(self):
+        return self.step >= self.base + self.nsteps and not self.pending and not self.in_batch
+
+    def choices(self):
+        opts = [("vis", i) for i in range(len(self.pending))]
+        if self.in_batch and not any(p.w0 < LL128_DATA_WORDS for p in self.pending):
+            opts.append(("fence",))
+        if (self.step < self.base + self.nsteps and len(self.in_batch) < self.batch
+                and all(st == self.step for (_, _, st) in self.in_batch)):
+            if not self.granted:
+                if all(self.step < self.f.heads[r] + self.f.N for r in self.rlanes):
+                    opts.append(("grant",))
+            else:
+                opts.append(("issue",))
+        return opts
+
+    def fire(self, choice):
+        if choice[0] == "grant":
+            self.granted = True
+        elif choice[0] == "issue":
+            rel = self.step - self.base
+            g0 = (rel * self.f.L + self.line) * LL128_DATA_WORDS
+            vals = [int(self.words[self.lo + g0 + j]) if g0 + j < self.nwords else 0
+                    for j in range(LL128_DATA_WORDS)]
+            k = self.step % self.f.N
+            for w0 in range(0, LL128_DATA_WORDS, self.pw):
+                self.pending.append(_Piece(k, self.line, w0, tuple(vals[w0:w0 + self.pw]), self.step))
+            self.in_batch.append((k, self.line, self.step))
+            self.line += 1
+            if self.line == self._end(self.step):
+                self.step += 1
+                self.line = self.l0
+                self.granted = False
+                self._skip_empty()
+        elif choice[0] == "fence":
+            for (k, ln, st) in self.in_batch:
+                self.pending.append(_Piece(k, ln, LL128_DATA_WORDS, (ll128_flag(st),), st))
+            self.in_batch = []
+            self._skip_empty()
+        else:
+            p = self.pending.pop(choice[1])
+            r = self.f.rlane(p.line)
+            if p.step >= self.f.heads[r] + self.f.N:
+                raise ProtocolViolation(f"LL128 step {p.step} overwrites line {p.line} of slot {p.slot} "
+                                        f"before receiver lane {r} returned it (head {self.f.heads[r]})")
+            n = len(p.values)
+            self.f.lines[p.slot, p.line, p.w0:p.w0 + n] = np.array(p.values, np.uint64)
+            self.f.owner[p.slot, p.line, p.w0:p.w0 + n] = p.step
+
+    def state(self):
+        return (self.step, self.line, self.granted, tuple(self.in_batch),
+                tuple((p.slot, p.line, p.w0, p.values, p.step) for p in self.pending))
+
+
+class LL128LaneReceiver(Actor):
+    """Receiver lane r: reads its lines of every slot-step, each only once
+    its flag is the step's (and then only words written in that step), and
+    publishes its head = step + 1 after its last line of the step (at once
+    for a step with none of its lines)."""
+
+    def __init__(self, fifo: LL128LaneFifo, out: np.ndarray, lo: int, hi: int, lane: int):
+        self.f, self.out, self.lo, self.hi, self.r = fifo, out, lo, hi, lane
+        self.nwords = hi - lo
+        self.base = fifo.heads[lane]
+        self.nsteps = ceil_div(self.nwords, fifo.L * LL128_DATA_WORDS)
+        self.l0 = min(lane * fifo.LgR, fifo.L)
+        self.l1 = min(self.l0 + fifo.LgR, fifo.L)
+        self.step = self.base
+        self.line = self.l0
+        self.name = f"ll128-recv-lane{lane}[{lo}:{hi}]"
+
+    def _end(self, step):
+        return min(self.l1, _ll128_lines(self.nwords, self.f.L, step - self.base))
+
+    def done(self):
+        return self.step >= self.base + self.nsteps
+
+    def choices(self):
+        if self.done():
+            return []
+        if self.line >= self._end(self.step):
+            return [("head",)]
+        k = self.step % self.f.N
+        return [("read",)] if int(self.f.lines[k, self.line, LL128_DATA_WORDS]) == ll128_flag(self.step) else []
+
+    def fire(self, choice):
+        if choice[0] == "head":
+            self.f.heads[self.r] = self.step + 1
+            self.step += 1
+            self.line = self.l0
+            return
+        k = self.step % self.f.N
+        own = self.f.owner[k, self.line, :LL128_DATA_WORDS]
+        stale = [int(o) for o in own if o != self.step]
+        if stale:
+            raise ProtocolViolation(f"LL128 line {self.line} of step {self.step} read with words from steps {stale}")
+        g0 = ((self.step - self.base) * self.f.L + self.line) * LL128_DATA_WORDS
+        n = min(LL128_DATA_WORDS, self.nwords - g0)
+        self.out[self.lo + g0:self.lo + g0 + n] = self.f.lines[k, self.line, :n]
+        self.line += 1
+
+    def state(self):
+        return (self.step, self.line)
+
+
 # --------------------------------------------------------------------------
 # Zero copy
 # --------------------------------------------------------------------------

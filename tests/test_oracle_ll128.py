@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import LL128Fifo, LL128Receiver, LL128Sender, ProtocolViolation, System, explore, ll128_flag
+from oracle import LL128Fifo, LL128Receiver, LL128Sender, ProtocolViolation, System, explore, ll128_flag, run
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -130,3 +130,51 @@ def test_ll128_result_independent_of_interleaving(seed):
     src = _bytes(5000, 42)
     out, _, _ = oracle.ll128_transfer(src, 2, 2, 384, seed=seed, batch=1 + seed % 3, piece_words=1 + seed)
     assert np.array_equal(out.view(np.uint8), src)
+
+
+# sender and receiver sides cut into different numbers of lanes (receiver
+# lanes with a head each; a sender lane waits for every receiver lane its
+# lines meet): the credit rule keeps every line from being overwritten before
+# the receiver lane that owns it has read it, whatever the interleaving
+
+def _lane_system(nlines, nslots, lines_per_slot, lanes, rlanes, fault=None, batch=1):
+    words = np.arange(1, nlines * 15 + 1, dtype=np.uint64)
+
+    def make():
+        f = oracle.LL128LaneFifo(nslots, lines_per_slot * 128, rlanes)
+        out = np.zeros_like(words)
+        actors = [oracle.LL128LaneSender(f, words, 0, len(words), lanes, g, batch=batch, fault=fault)
+                  for g in range(lanes)]
+        actors += [oracle.LL128LaneReceiver(f, out, 0, len(words), r) for r in range(rlanes)]
+        return System(actors, [f], [out])
+
+    def final(s):
+        assert np.array_equal(s.buffers[0], words)
+    return make, final
+
+
+@pytest.mark.parametrize("nlines,nslots,lps,lanes,rlanes", [
+    (4, 1, 2, 1, 2), (4, 1, 2, 2, 1), (6, 1, 3, 1, 3), (6, 1, 3, 3, 2), (6, 1, 3, 2, 2), (6, 2, 3, 2, 3),
+    (6, 2, 3, 3, 1), (9, 2, 3, 2, 2)])
+def test_ll128_lanes_exhaustive(nlines, nslots, lps, lanes, rlanes):
+    make, final = _lane_system(nlines, nslots, lps, lanes, rlanes)
+    assert explore(make, final) > 10
+
+
+@pytest.mark.parametrize("cfg", [(4, 1, 2, 1, 2), (6, 1, 3, 1, 3), (6, 1, 3, 2, 3)])
+def test_ll128_lane_credit_from_one_receiver_lane_is_caught(cfg):
+    # a sender lane whose lines meet two receiver lanes but that waits only
+    # for the first overwrites the second's lines in some interleaving
+    make, final = _lane_system(*cfg, fault="one_lane_credit")
+    with pytest.raises(ProtocolViolation):
+        explore(make, final)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_ll128_lanes_random_interleavings(seed):
+    # 8 lines a slot, 3 slots, 5 + 3 / 3 + 5 / 8 + 1 lanes, several steps
+    lanes, rlanes = [(5, 3), (3, 5), (8, 1)][seed % 3]
+    make, final = _lane_system(8 * 5 + 3, 3, 8, lanes, rlanes, batch=1 + seed % 2)
+    s = make()
+    run(s, seed=seed)
+    final(s)
