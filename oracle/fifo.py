@@ -39,6 +39,13 @@ Readings where the pages are silent:
   the sender writes chunks of at most S bytes, one tail per chunk, under the
   same credit rule; the receiver returns head per chunk; the sender empties
   ptrExchange once head reaches the last chunk.
+
+Our design beyond the pages (modelled so that its credit rule is checked):
+* LL128 lanes: a channel's lines are cut into G sender stripes and GR
+  receiver stripes of ceil(L / G) and ceil(L / GR) lines; each receiver
+  lane returns credit through a head of its own, and a sender lane fills
+  its lines of step s only once every receiver lane whose stripe meets its
+  own has head > s - N.
 """
 from __future__ import annotations
 
