@@ -69,18 +69,18 @@ def kernel_source_hash(sources=KERNEL_SOURCES, root: str = ROOT) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name: str = "p2p_tma_simple_1GiB_16ch", root: str = ROOT):
-    """DRAM bytes per launch of a kernel from its committed ncu record
-    (profiles/<name>.json), if the kernel's sources have not changed since it
-    was captured; else None."""
+def profiled_traffic(name: str = "p2p_tma_simple_1GiB_16ch", root: str = ROOT, field: str = "traffic_bytes_per_launch"):
+    """DRAM bytes (per launch, or another field of the record) of a kernel
+    from its committed ncu record (profiles/<name>.json), if the kernel's
+    sources have not changed since it was captured; else None."""
     try:
         rec = json.load(open(os.path.join(root, "profiles", name + ".json")))
         current = kernel_source_hash(rec.get("sources", KERNEL_SOURCES), root)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_source_hash") != current:
+    if rec.get("kernel_source_hash") != current or field not in rec:
         return None
-    return int(rec["traffic_bytes_per_launch"])
+    return int(rec[field])
 
 
 def time_stats(ms_list):
@@ -627,6 +627,12 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
                                       "gbs": n / (ms * 1e-3) / 1e9, "ms": ms, "ms_best": min(t), "ms_median": ms,
                                       "frac_of_hbm": (2 + 2 * 128 / 120) * n / (ms * 1e-3) / 1e9 / hbm_peak,
                                       "exact": bool(st2 == xp.XP_OK and torch.equal(dst, src))}
+            if (lanes, rlanes) == (4, 5):
+                # DRAM bytes of one launch from the committed ncu record of this configuration
+                dram = profiled_traffic("ll128_1GiB_16ch")
+                key = f"lanes{lanes}_recv{rlanes}"
+                multi[key]["dram_bytes_per_launch_ncu"] = dram
+                multi[key]["frac_dram"] = dram / (ms * 1e-3) / 1e9 / hbm_peak if dram else None
             xp.xp_fifo_destroy(f)
         res["ll128"] = {"us_per_message_with_launch": sweep, "sweep_status": st, "multi_1GiB_16ch": multi}
         del src, dst
@@ -739,6 +745,11 @@ def rows(torch, xp, hbm_peak, only=None, ring_mib=0):
                 "note": "frac_of_hbm counts the (6P-4)n bytes every slot write and read would move through DRAM; "
                         "FIFO lines that stay in L2 let it exceed 1, frac_of_ideal_2Pn is the bound",
                 "ranks_agree": bool(all(torch.equal(ys[0], y) for y in ys[1:])), "status": st}
+            if lanes == 0 and not ring_mib:
+                # DRAM bytes of one op from the committed ncu record of this configuration
+                dram = profiled_traffic("ring_tma_8ranks_f32", field="traffic_bytes_per_op")
+                ring["lanes_auto"]["dram_bytes_per_op_ncu"] = dram
+                ring["lanes_auto"]["frac_dram"] = dram / (ms * 1e-3) / 1e9 / hbm_peak if dram else None
             xp.xp_ring_destroy(r)
         res["ring_f32"] = ring
 
