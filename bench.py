@@ -251,7 +251,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--lanes", type=int, default=9, help="sender CTAs per channel")
-    ap.add_argument("--rlanes", type=int, default=9, help="receiver CTAs per channel")
+    ap.add_argument("--rlanes", type=int, default=10, help="receiver CTAs per channel")
     ap.add_argument("--no-rows", action="store_true", help="time the step only")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--mib", type=int, default=0,

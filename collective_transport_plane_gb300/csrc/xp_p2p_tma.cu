@@ -40,9 +40,9 @@
 // which does the release add on the arrival counter: a release waits for the
 // issuing thread's in-flight memory traffic, and the mover always has some.
 // A receiver stripe is signalled as soon as its bulk loads from the slot have
-// landed in shared memory.  Slot traffic is marked evict_last in L2 and
-// user-buffer traffic evict_first, so the FIFO stays L2-resident while src
-// and dst stream through.
+// landed in shared memory.  Slot traffic keeps L2's normal priority and
+// user-buffer traffic is marked evict_first, so the FIFO stays L2-resident
+// while src and dst stream through.
 #include <cuda_runtime.h>
 
 #include "xp_device.cuh"
@@ -277,7 +277,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) p2p_tma_kernel(const P2pParams
   // lanes and takes them back off (so the counters are zero between
   // operations).
   u64* arrivals = p.arr + (u64)ch * (kArrBytes / 8) + (sender ? 0 : kMaxSlots);
-  const u64 pol_slot = policy_evict_last();     // FIFO slots: reused every N steps
+  // FIFO slots: reused every N steps; normal priority (evict_last measured
+  // 1.7-3.7% slower on the 16-channel workload, evict_first 11% slower)
+  const u64 pol_slot = policy_evict_normal();
   // src / dst are read or written once: evict first where FIFO slots share the
   // L2 with them, normal priority where nothing else is kept (zero copy and
   // direct posts; measured 1-2% faster there, 9% slower for SIMPLE)

@@ -95,9 +95,9 @@ def test_simple_counters_continue(env):
     xp.xp_fifo_destroy(fifo)
 
 
-@pytest.mark.parametrize("lanes,rlanes", [(1, 1), (4, 4), (9, 9), (10, 8)])
+@pytest.mark.parametrize("lanes,rlanes", [(1, 1), (4, 4), (9, 9), (9, 10), (10, 8)])
 def test_simple_multichannel_workload(env, lanes, rlanes):
-    # 1 GiB of bf16 N(0,1), 16 channels of 8 x 512 KiB; 9 + 9 lanes with
+    # 1 GiB of bf16 N(0,1), 16 channels of 8 x 512 KiB; 9 + 10 lanes with
     # discards on is the configuration bench.py times, twice in a row
     torch, xp = env
     w = workloads.SIMPLE_MULTI
