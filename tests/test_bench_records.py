@@ -59,6 +59,19 @@ def test_committed_records_name_their_sources():
             assert os.path.exists(os.path.join(bench.ROOT, "collective_transport_plane_gb300", "csrc", f)), (name, f)
 
 
+def test_committed_records_match_their_summaries():
+    # each machine-readable record sits beside the text summary of the same
+    # capture, which names the same kernel source hash
+    prof = os.path.join(bench.ROOT, "profiles")
+    for name in os.listdir(prof):
+        if not name.endswith(".json"):
+            continue
+        rec = json.load(open(os.path.join(prof, name)))
+        md = os.path.join(prof, name[:-len(".json")] + ".md")
+        assert os.path.exists(md), name
+        assert rec["kernel_source_hash"] in open(md).read(), name
+
+
 def test_time_stats():
     st = bench.time_stats([0.5, 0.4, 0.7, 0.45])
     assert st["ms_best"] == 0.4
